@@ -1,0 +1,135 @@
+"""fp64 CPU oracle of the S6 selective-scan forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import this package. The product library never loads it: the CUDA
+path and this oracle share no code (no kernels, headers, helpers, tables or constants).
+
+The arithmetic lives in ``sscan_oracle.c`` (plain sequential loops in double precision, one
+POSIX thread per group of independent channels); this module compiles it with gcc and marshals
+numpy arrays to it. See the C file's header for what is computed and which page and section each
+step follows.
+
+Every function here has at least one pin in ``tests/test_oracle_pins.py`` against values the
+pages fix (the worked LTI demo of "架构变体：Mamba/SSM"), closed forms (causal convolution,
+the semiseparable-matrix form), invariants (Delta -> 0, associativity of the scan operator)
+and library routines (``numpy.logaddexp``, ``scipy.special.expit``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sscan_oracle.c")
+_LIB = os.path.join(_HERE, "libsscan_oracle.so")
+
+_lib_cache: dict = {}
+
+
+def build(mutant: int = 0, out: Optional[str] = None) -> str:
+    """Compile the C oracle with gcc (no fast-math: IEEE double semantics) and return its path.
+
+    ``mutant`` != 0 builds a deliberately broken copy; the pin tests use those copies to show
+    that each plausible mistake is caught by at least one pin.
+    """
+    if out is None:
+        out = _LIB if mutant == 0 else os.path.join(_HERE, f"libsscan_oracle_m{mutant}.so")
+    if mutant == 0 and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           f"-DSSCAN_ORACLE_MUTANT={int(mutant)}", "-o", out, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle shared library."""
+    path = path or build()
+    if path in _lib_cache:
+        return _lib_cache[path]
+    lib = ctypes.CDLL(path)
+    i64, vp, dp, fp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+    lib.sscan_oracle_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, dp, dp, dp,
+                                     i64, i64, i64, i64, ci, ci]
+    lib.sscan_oracle_fwd.restype = ci
+    lib.sscan_oracle_channel.argtypes = [vp, vp, vp, i64, fp, vp, vp, fp, fp, ci,
+                                         i64, i64, ci, dp, i64, dp, dp]
+    lib.sscan_oracle_channel.restype = None
+    _lib_cache[path] = lib
+    return lib
+
+
+def _io_array(a: np.ndarray, io: str) -> np.ndarray:
+    if io == "f32":
+        if a.dtype != np.float32:
+            raise TypeError(f"f32 io expects float32 arrays, got {a.dtype}")
+    elif io == "bf16":
+        if a.dtype != np.uint16:
+            raise TypeError(f"bf16 io expects the uint16 bit patterns, got {a.dtype}")
+    else:
+        raise ValueError(io)
+    return np.ascontiguousarray(a)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def fwd(u, delta, A, B, C, Dskip=None, z=None, delta_bias=None, softplus: bool = True,
+        io: str = "f32", threads: Optional[int] = None, want_mag: bool = False, lib=None):
+    """Selective-scan forward over whole tensors.
+
+    u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) float32; Dskip, delta_bias:
+    (dim,) float32. For ``io="bf16"`` the io tensors are uint16 arrays holding bf16 bit patterns.
+    Returns ``(y, h_last)`` as float64 arrays of shapes (batch, L, dim) and (batch, dim, N), plus
+    the absolute-value magnitude of every output when ``want_mag``.
+    """
+    lib = lib or load()
+    u, delta = _io_array(u, io), _io_array(delta, io)
+    B, C = _io_array(B, io), _io_array(C, io)
+    z = None if z is None else _io_array(z, io)
+    batch, L, dim = u.shape
+    N = B.shape[2]
+    assert delta.shape == u.shape and B.shape == C.shape == (batch, L, N)
+    assert z is None or z.shape == u.shape
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    assert A.shape == (dim, N)
+    Dskip = None if Dskip is None else np.ascontiguousarray(Dskip, dtype=np.float32)
+    delta_bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    y = np.empty((batch, L, dim), dtype=np.float64)
+    h = np.empty((batch, dim, N), dtype=np.float64)
+    mag = np.empty_like(y) if want_mag else None
+    nt = threads or os.cpu_count() or 1
+    rc = lib.sscan_oracle_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                              _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h),
+                              _ptr(mag), batch, L, dim, N, int(io == "bf16"), int(nt))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return (y, h, mag) if want_mag else (y, h)
+
+
+def fwd_channel(u, delta, A_d, B, C, Dskip_d=None, z=None, bias_d=None, softplus: bool = True,
+                io: str = "f32", want_mag: bool = False, lib=None):
+    """One channel: u, delta, z are (L,) io arrays, B and C (L, N), A_d (N,) float32, Dskip_d and
+    bias_d Python floats (stored as float32) or None. Returns ``(y (L,), h_last (N,))`` in float64
+    (plus the magnitude when ``want_mag``). Used to check sampled channels of large runs."""
+    lib = lib or load()
+    u, delta = _io_array(u, io), _io_array(delta, io)
+    B, C = _io_array(B, io), _io_array(C, io)
+    z = None if z is None else _io_array(z, io)
+    L = u.shape[0]
+    N = B.shape[1]
+    A_d = np.ascontiguousarray(A_d, dtype=np.float32)
+    Dv = None if Dskip_d is None else np.array([Dskip_d], dtype=np.float32)
+    bv = None if bias_d is None else np.array([bias_d], dtype=np.float32)
+    y = np.empty(L, dtype=np.float64)
+    h = np.empty(N, dtype=np.float64)
+    mag = np.empty(L, dtype=np.float64) if want_mag else None
+    lib.sscan_oracle_channel(_ptr(u), _ptr(delta), _ptr(z), 1, _ptr(A_d), _ptr(B), _ptr(C),
+                             _ptr(Dv), _ptr(bv), int(bool(softplus)), L, N, int(io == "bf16"),
+                             _ptr(y), 1, _ptr(h), _ptr(mag))
+    return (y, h, mag) if want_mag else (y, h)
