@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the S6 selective-scan forward (libsscan) on B300.
+
+One step = one selective-scan forward over the whole workload (softplus, discretisation,
+recurrence, readout, skip, gate, h_last) = one kernel launch. Default workload: fp32, batch 8,
+L 2048, D 1536 (d_model 768, expand 2), N 16, z gate, D skip, h_last returned.
+
+Prints ONE JSON line (rank 0). Under torchrun with N ranks every rank runs its own full replica
+of the workload on its own GPU (the batch rows and channels are independent; no data-path
+collective), the timed region is bracketed by a barrier and a device synchronize, and the
+slowest rank's time is used: value = N * units / max_time ("scaling": "weak").
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on a bounded sample of
+the same workload per step, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan fwd GB/s and (B·L·D·N)/s on 1 B300; % of HBM/SFU roofline"
+UNIT = "(B*L*D*N)/s"
+SFU_EX2_PER_CLK_PER_SM = 32  # MUFU.EX2 lanes per SM per clock on B300 (measured by our probe)
+FALLBACK_HBM_GBS = 6400.0
+L2_BYTES = 126 * 2**20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["lib", "reference"], default="lib")
+    ap.add_argument("--workload", default="fp32")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2032.0)), "measured"
+    return FALLBACK_HBM_GBS, 2032.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_158_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel
+    source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(workload_key)
+    if not d or d.get("source_sha") != kernel_source_sha():
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event (throttle) reasons while the timed region runs, with
+    NVML if the Python bindings import, else by streaming `nvidia-smi -lms`."""
+
+    REASONS = {
+        "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sync_boost": 0x10,
+        "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40, "hw_power_brake": 0x80,
+    }
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index = index
+        self.period_ms = period_ms
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.source = None
+        self.err = None
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.source = "nvml"
+        except Exception as e:
+            self.err = repr(e)
+            self.source = "nvidia-smi"
+
+    def _run_nvml(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period_ms / 1e3)
+
+    def _run_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:
+            self.err = repr(e)
+            return
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                self.samples.append(float(parts[0]))
+                self.max_mhz = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    self.reasons.add(n)
+
+    def __enter__(self):
+        target = self._run_nvml if self.source == "nvml" else self._run_smi
+        self.t = threading.Thread(target=target, daemon=True)
+        self.t.start()
+        if self.source == "nvidia-smi":
+            time.sleep(0.3)  # let nvidia-smi start before the timed region
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if getattr(self, "proc", None) is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.t.join(timeout=5)
+
+    def summary(self):
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples), "source": self.source}
+        if not self.samples and self.err:
+            out["note"] = f"no clock samples: {self.err}"
+        return out
+
+    def rejected(self):
+        bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+        if self.reasons & bad:
+            return True
+        s = self.summary()
+        if s["sm_mhz"] and s["sm_max_mhz"] and s["sm_mhz"] < 0.6 * s["sm_max_mhz"] and \
+                not (self.reasons - {"sync_boost"}):
+            return True
+        return False
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(w, x, seconds: float):
+    """The oracle, as it stands, on a bounded sample of the workload: whole batch rows (or the
+    first k channels of row 0) over the full sequence, sized for about `seconds` of wall time."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    cores = os.cpu_count() or 1
+
+    def io(t):
+        if t is None:
+            return None
+        t = t.cpu().contiguous()
+        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
+
+    def run(rows, k):
+        sl = lambda name: None if x.get(name) is None else x[name][0:rows, :, :k]  # noqa: E731
+        args = (io(sl("u")), io(sl("delta")), x["A"][:k].cpu().numpy(), io(x["B"][0:rows]),
+                io(x["C"][0:rows]), None if x.get("D") is None else x["D"][:k].cpu().numpy(),
+                io(sl("z")),
+                None if x.get("delta_bias") is None else x["delta_bias"][:k].cpu().numpy())
+        t0 = time.perf_counter()
+        oracle.fwd(*args, io=w.io, threads=cores)
+        return time.perf_counter() - t0
+
+    k = min(w.dim, max(4 * cores, 32))
+    t = run(1, k)
+    target = w.L * k * w.N * seconds / max(t, 1e-3)  # updates that fill the time budget
+    row_units = w.L * w.dim * w.N
+    if target >= row_units:
+        rows, k = int(min(w.batch, max(1, target // row_units))), w.dim
+    else:
+        rows, k = 1, int(min(w.dim, max(k, target // (w.L * w.N))))
+    t2 = run(rows, k)
+    units = rows * w.L * k * w.N
+    return {"value": units / t2, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"batch rows 0..{rows - 1} of {w.batch}, channels 0..{k - 1} of {w.dim}, "
+                      f"full L={w.L}, N={w.N}: {units:.3g} updates in {t2:.2f} s "
+                      f"(fp64 C loop, {cores} threads)"}
+
+
+def run_reference(args, w):
+    """--impl reference: the oracle timed per step on a bounded sample (rank 0 only)."""
+    world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from selective_state_space_158_b300.inputs import make_inputs
+
+    oracle.build()
+    # The sample's inputs come from the same seeded recipe, drawn for one batch row and a
+    # channel slice on the CPU (the oracle needs no device).
+    cores = os.cpu_count() or 1
+    budget = 120.0  # seconds for the whole run
+    per_step = budget / max(1, args.steps + args.warmup)
+    k = 1
+    sub = w.replace(batch=1, dim=max(1, min(w.dim, 64)))
+    x = make_inputs(sub, device="cpu")
+    import numpy as np
+
+    def io(t):
+        if t is None:
+            return None
+        t = t.contiguous()
+        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
+
+    def step(k):
+        sl = lambda n: None if x.get(n) is None else x[n][:, :, :k]  # noqa: E731
+        oracle.fwd(io(sl("u")), io(sl("delta")), x["A"][:k].numpy(), io(x["B"]), io(x["C"]),
+                   None if x.get("D") is None else x["D"][:k].numpy(), io(sl("z")),
+                   None if x.get("delta_bias") is None else x["delta_bias"][:k].numpy(),
+                   io=w.io, threads=cores)
+
+    t0 = time.perf_counter()
+    step(1)
+    t1 = time.perf_counter() - t0
+    k = int(max(1, min(sub.dim, per_step / max(t1, 1e-5))))
+    for _ in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(k)
+    el = time.perf_counter() - t0
+    units = args.steps * w.L * k * w.N
+    val = units / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": config_of(w),
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: batch row 0, channels 0..{k - 1}, full L={w.L}"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.dim, "N": w.N, "io": w.io,
+            "A": "-(n+1)" if w.A_kind == "neg_n1" else "-exp(U(log1,log16))",
+            "step_range": list(w.dt_range), "z_gate": w.has_z, "D_skip": w.has_D,
+            "h_last": True, "parallelism": "replica per GPU",
+            "l2": f"inputs larger than L2 ({w.io_bytes() / 1e6:.0f} MB footprint vs 126 MiB L2)"}
+
+
+def main():
+    args = parse_args()
+    from selective_state_space_158_b300.inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from selective_state_space_158_b300 import binding
+    from selective_state_space_158_b300.inputs import make_inputs
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    binding.load()  # fails loudly if the library is missing
+
+    x = make_inputs(w, device=dev)
+    y = torch.empty_like(x["u"])
+    h = torch.empty((w.batch, w.dim, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        binding.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x.get("D"), x.get("z"),
+                    x.get("delta_bias"), y=y, h_last=h, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(K):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as cs:
+            ev0.record(stream)
+            for _ in range(K):
+                step()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        return ms, cs
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if binding.device_error(stream) != 0:
+        raise RuntimeError("device-side error during warm-up")
+    ms, cs = timed(args.steps)
+    remeasured = False
+    if cs.rejected():
+        ms, cs = timed(args.steps)
+        remeasured = True
+    if binding.device_error(stream) != 0:
+        raise RuntimeError("device-side error during the timed region")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    sec_per_step = ms_max / 1e3 / args.steps
+    value = world * w.elems / sec_per_step
+
+    # ---- roofline of the (only) kernel: one launch per step, timed on its own stream ----
+    hbm_gbs, sm_max_mhz, peak_src = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    alu_peak = sms * SFU_EX2_PER_CLK_PER_SM * sm_max_mhz * 1e6  # ex2 (= updates) per second
+    per_launch_s = ms / 1e3 / args.steps
+    bytes_ = w.io_bytes()
+    gbs = bytes_ / per_launch_s / 1e9
+    t_hbm = bytes_ / (hbm_gbs * 1e9)
+    t_alu = w.elems / alu_peak
+    traffic = recorded_traffic(args.workload)
+    if t_hbm >= t_alu:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": gbs / hbm_gbs, "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"}
+    else:
+        ach = w.elems / per_launch_s
+        roof = {"bound": "alu", "achieved": ach / 1e9, "peak": alu_peak / 1e9,
+                "unit": "G ex2/s (SFU)", "frac": ach / alu_peak, "traffic": traffic,
+                "peak_source": f"{sms} SMs x {SFU_EX2_PER_CLK_PER_SM} ex2/clk x {sm_max_mhz:.0f} MHz"}
+    roof["hbm_frac"] = gbs / hbm_gbs
+    roof["sfu_frac"] = (w.elems / per_launch_s) / alu_peak
+    clocks = cs.summary()
+    if clocks.get("sm_mhz"):
+        roof["sfu_frac_at_observed_clock"] = (w.elems / per_launch_s) / (
+            sms * SFU_EX2_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.io, "data": "synthetic (seeded)",
+        "config": config_of(w), "gbs": gbs * world, "gpu_launches": args.steps,
+        "roofline": roof, "clocks": clocks,
+    }
+    if remeasured:
+        line["clocks"]["note"] = "first measurement rejected by clock check; re-measured once"
+
+    # ---- end to end through the host-buffer C entry point ----
+    if not args.no_e2e:
+        xh = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+        yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        hh = torch.empty(h.shape, dtype=h.dtype).pin_memory()
+
+        def e2e_step():
+            binding.fwd_host(xh["u"], xh["delta"], xh["A"], xh["B"], xh["C"], xh.get("D"),
+                             xh.get("z"), xh.get("delta_bias"), y=yh, h_last=hh, device=local,
+                             stream=stream)
+
+        for _ in range(2):
+            e2e_step()
+        K2 = max(3, args.e2e_steps)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(K2):
+            e2e_step()
+        el = time.perf_counter() - t0
+        te = torch.tensor([el], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        el = float(te.item())
+        es = 4 if w.io == "f32" else 2
+        bld, bln = w.batch * w.L * w.dim, w.batch * w.L * w.N
+        h2d = bld * es * (2 + int(w.has_z)) + 2 * bln * es + w.dim * w.N * 4 + \
+            w.dim * 4 * (int(w.has_D) + int(w.has_bias))
+        d2h = bld * es + w.batch * w.dim * w.N * 4
+        line["e2e"] = {"value": world * w.elems * K2 / el, "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "steps": K2, "ms_per_step": el / K2 * 1e3,
+                       "api": "sscan_fwd_host (pinned host buffers, copies inside the region)"}
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,98 @@
+/*
+ * sscan.h -- C ABI of libsscan, the S6 selective-scan forward on NVIDIA B300 (sm_103a).
+ *
+ * The operation (pages cited by title and section):
+ *   "Mamba：选择性状态空间模型入门教程", section "Mamba 的关键创新：选择性机制" (selective scan
+ *   pseudo-code); "Mamba: Linear-Time Sequence Modeling with Selective State Spaces" (wiki notes),
+ *   section "核心贡献：选择机制（S6）" (B_t, C_t of shape (B, L, N), Delta_t = tau(Delta + s(x_t)));
+ *   "架构变体：Mamba/SSM", sections "离散化" (zero-order hold) and "硬件感知算法" (one fused scan,
+ *   state kept on chip).
+ *
+ * For every batch row b, channel d and step t = 0 .. L-1, with h[b,d,:] = 0 before t = 0:
+ *   dt          = softplus_flag ? log(1 + exp(delta[b,t,d] + bias[d])) : delta[b,t,d] + bias[d]
+ *   h[b,d,n]    = exp(dt * A[d,n]) * h[b,d,n] + dt * B[b,t,n] * u[b,t,d]      (n = 0 .. N-1)
+ *   y[b,t,d]    = sum_n C[b,t,n] * h[b,d,n] + D[d] * u[b,t,d]
+ *   y[b,t,d]   *= z[b,t,d] / (1 + exp(-z[b,t,d]))                             (only if z given)
+ *   h_last[b,d,n] = h[b,d,n] after step L-1
+ * State and arithmetic are fp32; inputs and y are fp32 or bf16 (dtype).
+ */
+#ifndef SSCAN_H
+#define SSCAN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSCAN_F32 = 0, SSCAN_BF16 = 1 } sscan_dtype_t;
+
+typedef enum {
+  SSCAN_OK = 0,
+  SSCAN_ERR_INVALID_ARG = 1,   /* null required pointer, negative size, N outside 1..16, ... */
+  SSCAN_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (no such case today) */
+  SSCAN_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  SSCAN_ERR_CARRY_TIMEOUT = 4  /* device side: a chunk-carry wait ran out of its bound */
+} sscan_status_t;
+
+/*
+ * sscan_fwd -- selective-scan forward on device memory, asynchronous on `stream`.
+ *
+ * Pointers (all device memory owned by the caller; the library keeps none after returning):
+ *   u, delta, z : (batch, L, dim) row-major, dim fastest, element type `dtype`
+ *   A           : (dim, N) fp32 (the continuous-time diagonal state matrix, normally < 0)
+ *   B, C        : (batch, L, N) row-major, N fastest, element type `dtype` (shared over dim)
+ *   D           : (dim) fp32 skip weights, or NULL for no skip term
+ *   z           : gate input, or NULL for no SiLU gate
+ *   delta_bias  : (dim) fp32, or NULL for a zero bias
+ *   y           : (batch, L, dim) output, element type `dtype`; must not alias any input
+ *   h_last      : (batch, dim, N) fp32 final state, or NULL if not wanted
+ * softplus_flag != 0 applies softplus to delta + bias; 0 uses delta + bias as the step.
+ * Sizes: batch, L, dim >= 0; 1 <= N <= 16. batch, L or dim = 0 is a no-op that returns
+ * SSCAN_OK (h_last, if given, is zeroed when L = 0).
+ * Any alignment and any dim are accepted; 16-byte aligned pointers with dim and N multiples of
+ * 4 (fp32) or 8 (bf16) take the TMA-staged fast path, anything else a plain-load path.
+ *
+ * Errors: argument checks are synchronous and return SSCAN_ERR_INVALID_ARG before anything is
+ * launched; launch failures return SSCAN_ERR_CUDA. A device-side carry timeout (possible only
+ * when the library splits one sequence across thread blocks) is recorded in a per-device status
+ * word that sscan_get_device_error reports.
+ * Workspace: when a sequence is split across thread blocks the library takes a small
+ * stream-ordered scratch allocation (cudaMallocAsync on `stream`) and frees it stream-ordered.
+ */
+sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus_flag, void* y, float* h_last, int64_t batch, int64_t L,
+                         int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * sscan_fwd_host -- the same operation on HOST buffers: copies the inputs to the current
+ * device on `stream`, runs sscan_fwd, copies y and h_last back and synchronizes `stream`.
+ * Arguments mean what they mean for sscan_fwd but every pointer is host memory (page-locked
+ * memory gives asynchronous, overlapped copies). Device staging buffers are owned by the library
+ * per device, grown on demand and kept until sscan_release(). Returns when y and h_last hold the
+ * result, or with the first error.
+ */
+sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus_flag, void* y, float* h_last,
+                              int64_t batch, int64_t L, int64_t dim, int64_t N,
+                              sscan_dtype_t dtype, cudaStream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the current device's status word (set by
+ * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT). Returns SSCAN_OK if clear. */
+sscan_status_t sscan_get_device_error(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sscan_status_string(sscan_status_t status);
+
+/* Frees the library's per-device buffers (status word, host-path staging) on the current
+ * device. Call only when no sscan work is in flight on that device. */
+sscan_status_t sscan_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSCAN_H */

@@ -1,0 +1,164 @@
+"""Thin ctypes binding of libsscan: argument marshalling only.
+
+Every step of the scan runs in the library's CUDA kernels; this module only checks tensor
+properties, passes ``data_ptr()`` values and the current CUDA stream to the C entry points, and
+turns status codes into exceptions. There is no fallback: if ``libsscan.so`` is missing or no
+CUDA device is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsscan.so")
+
+SSCAN_F32, SSCAN_BF16 = 0, 1
+STATUS = {0: "SSCAN_OK", 1: "SSCAN_ERR_INVALID_ARG", 2: "SSCAN_ERR_UNSUPPORTED",
+          3: "SSCAN_ERR_CUDA", 4: "SSCAN_ERR_CARRY_TIMEOUT"}
+
+# Every symbol include/sscan.h declares, with its ctypes signature.
+_vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+_FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i64, _i64, _i64,
+             _int, _vp]
+SIGNATURES = {
+    "sscan_fwd": (_FWD_ARGS, _int),
+    "sscan_fwd_host": (_FWD_ARGS, _int),
+    "sscan_get_device_error": ([_vp], _int),
+    "sscan_status_string": ([_int], ctypes.c_char_p),
+    "sscan_release": ([], _int),
+}
+
+_lib = None
+
+
+class SscanError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libsscan.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise OSError(f"libsscan.so not built at {p}; run selective_state_space_158_b300.build")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SscanError(code, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSCAN_F32
+    if t.dtype == torch.bfloat16:
+        return SSCAN_BF16
+    raise TypeError(f"io tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+        C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+        delta_bias: Optional[torch.Tensor] = None, softplus: bool = True,
+        y: Optional[torch.Tensor] = None, h_last: Optional[torch.Tensor] = None,
+        return_last_state: bool = True, stream=None):
+    """Selective-scan forward on CUDA tensors (asynchronous on ``stream`` or the current stream).
+
+    u, delta, z: (batch, L, dim); B, C: (batch, L, N) with 1 <= N <= 16, all of one io dtype
+    (float32 or bfloat16); A: (dim, N) float32; D, delta_bias: (dim,) float32.
+    Returns ``y`` (batch, L, dim) in the io dtype and, if ``return_last_state``, ``h_last``
+    (batch, dim, N) float32.
+    """
+    lib = load()
+    io = _dtype_code(u)
+    batch, L, dim = u.shape
+    N = B.shape[-1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("libsscan computes on CUDA tensors only")
+    for name, t, shape, dt in [("delta", delta, (batch, L, dim), u.dtype),
+                               ("B", B, (batch, L, N), u.dtype), ("C", C, (batch, L, N), u.dtype),
+                               ("A", A, (dim, N), torch.float32)]:
+        if tuple(t.shape) != shape or t.dtype != dt or t.device != dev:
+            raise ValueError(f"{name}: expected {shape} {dt} on {dev}, got "
+                             f"{tuple(t.shape)} {t.dtype} on {t.device}")
+    for name, t, shape, dt in [("D", D, (dim,), torch.float32), ("z", z, (batch, L, dim), u.dtype),
+                               ("delta_bias", delta_bias, (dim,), torch.float32)]:
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dt or t.device != dev):
+            raise ValueError(f"{name}: expected {shape} {dt} on {dev}")
+    ts = [u, delta, A, B, C, D, z, delta_bias]
+    if any(t is not None and not t.is_contiguous() for t in ts):
+        raise ValueError("all tensors must be contiguous")
+    if y is None:
+        y = torch.empty_like(u)
+    if return_last_state and h_last is None:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        code = lib.sscan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                             _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),
+                             batch, L, dim, N, io, _stream_handle(stream, dev))
+    _check(code, "sscan_fwd")
+    return (y, h_last) if return_last_state else y
+
+
+def fwd_host(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, D=None, z=None, delta_bias=None, softplus: bool = True,
+             y: Optional[torch.Tensor] = None, h_last: Optional[torch.Tensor] = None,
+             device: int = 0, stream=None):
+    """The same operation on CPU tensors (pinned memory recommended): the library copies the
+    inputs to ``device``, scans, copies y and h_last back and synchronizes. Returns (y, h_last)."""
+    lib = load()
+    io = _dtype_code(u)
+    batch, L, dim = u.shape
+    N = B.shape[-1]
+    ts = [u, delta, A, B, C, D, z, delta_bias]
+    if any(t is not None and (t.device.type != "cpu" or not t.is_contiguous()) for t in ts):
+        raise ValueError("fwd_host takes contiguous CPU tensors")
+    if y is None:
+        y = torch.empty_like(u)
+    if h_last is None:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32)
+    dev = torch.device("cuda", device)
+    with torch.cuda.device(dev):
+        code = lib.sscan_fwd_host(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                  _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y),
+                                  _ptr(h_last), batch, L, dim, N, io,
+                                  _stream_handle(stream, dev))
+    _check(code, "sscan_fwd_host")
+    return y, h_last
+
+
+def device_error(stream=None, device=None) -> int:
+    """Synchronize and return (then clear) the device status word; 0 means no device error."""
+    lib = load()
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return lib.sscan_get_device_error(_stream_handle(stream, dev))
+
+
+def status_string(code: int) -> str:
+    return load().sscan_status_string(code).decode()

@@ -1,0 +1,221 @@
+// sscan_api.cu -- the C ABI of libsscan: argument checks, path choice, per-device state and the
+// host-buffer entry point. The operation itself is defined in include/sscan.h.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sscan.h"
+#include "sscan_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  unsigned int* status = nullptr;  // device status word
+  // host-path staging (device side), grown on demand
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+unsigned int* status_word(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.status) {
+    if (cudaMalloc(&s.status, sizeof(unsigned int)) != cudaSuccess) {
+      s.status = nullptr;
+      return nullptr;
+    }
+    if (cudaMemset(s.status, 0, sizeof(unsigned int)) != cudaSuccess) return nullptr;
+  }
+  return s.status;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+// Shared validation of sizes and pointer presence; fills the element counts.
+sscan_status_t check_args(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
+                          int64_t N, sscan_dtype_t dtype, int64_t* n_bld, int64_t* n_bln) {
+  if (dtype != SSCAN_F32 && dtype != SSCAN_BF16) return SSCAN_ERR_INVALID_ARG;
+  if (batch < 0 || L < 0 || dim < 0 || N < 1 || N > 16) return SSCAN_ERR_INVALID_ARG;
+  int64_t bl, bld, bln, bd, bdn, bytes;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, dim, &bld) || !mul_ok(bl, N, &bln) ||
+      !mul_ok(bld, 4, &bytes) || !mul_ok(batch, dim, &bd) || !mul_ok(bd, N, &bdn) ||
+      !mul_ok(bdn, 4, &bytes))
+    return SSCAN_ERR_INVALID_ARG;
+  *n_bld = bld;
+  *n_bln = bln;
+  if (bd == 0 || L == 0) return SSCAN_OK;  // nothing to read
+  if (!A || !u || !delta || !B || !C || !y) return SSCAN_ERR_INVALID_ARG;
+  return SSCAN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sscan_status_string(sscan_status_t s) {
+  switch (s) {
+    case SSCAN_OK: return "SSCAN_OK";
+    case SSCAN_ERR_INVALID_ARG: return "SSCAN_ERR_INVALID_ARG";
+    case SSCAN_ERR_UNSUPPORTED: return "SSCAN_ERR_UNSUPPORTED";
+    case SSCAN_ERR_CUDA: return "SSCAN_ERR_CUDA";
+    case SSCAN_ERR_CARRY_TIMEOUT: return "SSCAN_ERR_CARRY_TIMEOUT";
+  }
+  return "SSCAN_ERR_UNKNOWN";
+}
+
+sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus_flag, void* y, float* h_last, int64_t batch, int64_t L,
+                         int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream) {
+  int64_t bld = 0, bln = 0;
+  sscan_status_t st = check_args(u, delta, A, B, C, y, batch, L, dim, N, dtype, &bld, &bln);
+  if (st != SSCAN_OK) return st;
+  const int dev = current_device();
+  if (dev < 0) return SSCAN_ERR_CUDA;
+  if (batch == 0 || dim == 0) return SSCAN_OK;
+  if (L == 0) {
+    if (h_last &&
+        cudaMemsetAsync(h_last, 0, size_t(batch * dim * N) * sizeof(float), stream) != cudaSuccess)
+      return SSCAN_ERR_CUDA;
+    return SSCAN_OK;
+  }
+  sscan::FwdArgs a;
+  a.u = u;
+  a.delta = delta;
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.D = D;
+  a.z = z;
+  a.bias = delta_bias;
+  a.softplus = softplus_flag != 0;
+  a.y = y;
+  a.h_last = h_last;
+  a.batch = batch;
+  a.L = L;
+  a.dim = dim;
+  a.N = N;
+  a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
+  a.stream = stream;
+  a.status = status_word(dev);
+  if (!a.status) return SSCAN_ERR_CUDA;
+  cudaError_t e;
+  const char* force = std::getenv("SSCAN_PATH");
+  const bool want_simple = force && std::strcmp(force, "simple") == 0;
+  if (!want_simple && sscan::tma_path_ok(a))
+    e = sscan::launch_tma(a, sscan::tuning_from_env());
+  else
+    e = sscan::launch_simple(a);
+  return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
+sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus_flag, void* y, float* h_last,
+                              int64_t batch, int64_t L, int64_t dim, int64_t N,
+                              sscan_dtype_t dtype, cudaStream_t stream) {
+  int64_t bld = 0, bln = 0;
+  sscan_status_t st = check_args(u, delta, A, B, C, y, batch, L, dim, N, dtype, &bld, &bln);
+  if (st != SSCAN_OK) return st;
+  const int dev = current_device();
+  if (dev < 0) return SSCAN_ERR_CUDA;
+  if (batch == 0 || dim == 0) return SSCAN_OK;
+  const size_t es = dtype == SSCAN_F32 ? 4 : 2;
+  // Device staging layout, each piece 256-byte aligned.
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t s_bld = up(size_t(bld) * es), s_bln = up(size_t(bln) * es);
+  const size_t s_A = up(size_t(dim * N) * 4), s_dim = up(size_t(dim) * 4);
+  const size_t s_h = up(size_t(batch * dim * N) * 4);
+  const size_t total = (3 + (z ? 1 : 0)) * s_bld + 2 * s_bln + s_A + 2 * s_dim + s_h;
+  unsigned char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& ds = g_dev[dev];
+    if (ds.stage_bytes < total) {
+      if (ds.stage) {
+        cudaStreamSynchronize(stream);
+        cudaFree(ds.stage);
+      }
+      ds.stage = nullptr;
+      ds.stage_bytes = 0;
+      if (cudaMalloc(&ds.stage, total) != cudaSuccess) return SSCAN_ERR_CUDA;
+      ds.stage_bytes = total;
+    }
+    base = static_cast<unsigned char*>(ds.stage);
+  }
+  unsigned char* p = base;
+  auto take = [&](size_t n) { unsigned char* r = p; p += n; return r; };
+  void* du = take(s_bld);
+  void* ddl = take(s_bld);
+  void* dy = take(s_bld);
+  void* dz = z ? take(s_bld) : nullptr;
+  void* dB = take(s_bln);
+  void* dC = take(s_bln);
+  float* dA = reinterpret_cast<float*>(take(s_A));
+  float* dD = D ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
+  float* dbias = delta_bias ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
+  float* dh = h_last ? reinterpret_cast<float*>(take(s_h)) : nullptr;
+  auto h2d = [&](void* dst, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  };
+  const size_t nb = size_t(bld) * es, nbc = size_t(bln) * es;
+  bool ok = h2d(du, u, nb) && h2d(ddl, delta, nb) && (!z || h2d(dz, z, nb)) &&
+            h2d(dB, B, nbc) && h2d(dC, C, nbc) && h2d(dA, A, size_t(dim * N) * 4) &&
+            (!D || h2d(dD, D, size_t(dim) * 4)) &&
+            (!delta_bias || h2d(dbias, delta_bias, size_t(dim) * 4));
+  if (!ok) return SSCAN_ERR_CUDA;
+  st = sscan_fwd(du, ddl, dA, dB, dC, dD, dz, dbias, softplus_flag, dy, dh, batch, L, dim, N,
+                 dtype, stream);
+  if (st != SSCAN_OK) return st;
+  if (nb && cudaMemcpyAsync(y, dy, nb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return SSCAN_ERR_CUDA;
+  if (h_last && cudaMemcpyAsync(h_last, dh, size_t(batch * dim * N) * 4, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess)
+    return SSCAN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SSCAN_ERR_CUDA;
+  return SSCAN_OK;
+}
+
+sscan_status_t sscan_get_device_error(cudaStream_t stream) {
+  const int dev = current_device();
+  if (dev < 0) return SSCAN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SSCAN_ERR_CUDA;
+  unsigned int* w = status_word(dev);
+  if (!w) return SSCAN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SSCAN_ERR_CUDA;
+  if (v == 0) return SSCAN_OK;
+  if (cudaMemset(w, 0, sizeof v) != cudaSuccess) return SSCAN_ERR_CUDA;
+  return SSCAN_ERR_CARRY_TIMEOUT;
+}
+
+sscan_status_t sscan_release(void) {
+  const int dev = current_device();
+  if (dev < 0) return SSCAN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  cudaError_t e = cudaSuccess;
+  if (s.status) e = cudaFree(s.status);
+  if (s.stage && e == cudaSuccess) e = cudaFree(s.stage);
+  s = DeviceState();
+  return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// sscan_device.cuh -- device-side building blocks of libsscan (sm_103a): inline-PTX wrappers for
+// mbarriers, TMA tensor copies and the SFU exponential, io-type conversions, and the scalar
+// per-(step, channel) functions (softplus, SiLU) in scalar and f32x2-paired forms.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sscan {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- io element conversions -------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_io(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_io(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---- SFU exponential: 2^x, flushing denormal results to zero ----------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- paired (f32x2) forms used per (step, channel pair) ------------------------------------
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// log1p(s)/s on [0, 1]: degree-9 polynomial from Chebyshev interpolation in double precision,
+// re-expanded in powers of s and rounded to fp32 (csrc/gen_softplus_poly.py regenerates it).
+// s * p(s) matches log1p(s) to 1.6e-7 relative in fp32 on the whole interval.
+__device__ __forceinline__ float2 log1p_unit2(float2 s) {
+  constexpr float c[10] = {1.000000000e+00f, -4.999989271e-01f, 3.332971036e-01f,
+                           -2.495161593e-01f, 1.966327429e-01f, -1.526966691e-01f,
+                           1.054362357e-01f, -5.637361482e-02f, 1.954252832e-02f,
+                           -3.176057013e-03f};
+  float2 acc = f2(c[9], c[9]);
+#pragma unroll
+  for (int i = 8; i >= 0; --i) acc = __ffma2_rn(acc, s, f2(c[i], c[i]));
+  return __fmul2_rn(s, acc);
+}
+
+// Argument shift for the decay factor 2^(dt * A * log2 e). Measured on B300 (sm_103a), the SFU's
+// ex2.approx.ftz.f32 returns results that are on average 0.1-0.2 ulp low for arguments in
+// [-3e-3, 0) and up to 0.5 ulp low near -1e-2. A decay factor is multiplied into the state at
+// every step, so a consistently low factor compounds over the state's memory (hundreds to
+// thousands of steps for small dt). Adding 1e-8 to the argument (for free: the product becomes
+// an FMA) centres the error on zero for the slow-decay arguments where compounding matters.
+constexpr float kEx2ArgShift = 1.0e-8f;
+
+// softplus on a pair: max(x, 0) + log1p(exp(-|x|)); one SFU exponential per element.
+__device__ __forceinline__ float2 softplus2(float2 x) {
+  const float2 e = __fmul2_rn(f2(-fabsf(x.x), -fabsf(x.y)), f2(kLog2e, kLog2e));
+  const float2 s = f2(ex2(e.x), ex2(e.y));
+  return __fadd2_rn(f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2(s));
+}
+
+// softplus(x) = log(1 + e^x), the positivity map of the step ("Mamba：选择性状态空间模型入门教程",
+// selective-scan pseudo-code), scalar form of softplus2.
+__device__ __forceinline__ float softplus_f(float x) {
+  const float2 r = softplus2(f2(x, 0.f));
+  return r.x;
+}
+
+// SiLU on a pair: z / (1 + 2^(-z log2 e)).
+__device__ __forceinline__ float2 silu2(float2 z) {
+  const float2 e = __fmul2_rn(z, f2(-kLog2e, -kLog2e));
+  const float2 d = __fadd2_rn(f2(ex2(e.x), ex2(e.y)), f2(1.f, 1.f));
+  return f2(__fdividef(z.x, d.x), __fdividef(z.y, d.y));
+}
+
+// z * sigmoid(z), the SiLU gate of the Mamba block ("Mamba: Linear-Time Sequence Modeling with
+// Selective State Spaces", block diagram in "架构：极简设计").
+__device__ __forceinline__ float silu_f(float z) {
+  return __fdividef(z, 1.f + ex2(-z * kLog2e));
+}
+
+// ---- io pairs ---------------------------------------------------------------------------------
+__device__ __forceinline__ float2 load_pair(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void store_pair(float* p, float2 v) {
+  *reinterpret_cast<float2*>(p) = v;
+}
+__device__ __forceinline__ void store_pair(__nv_bfloat16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
+}
+
+// ---- shared-memory addresses ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ---------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: returns false if the phase did not complete within `max_tries` polls (each poll
+// may itself suspend the thread for a hardware-chosen interval).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t max_tries) {
+  for (uint32_t i = 0; i < max_tries; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+// ---- TMA tensor copies (3-D maps: x = fastest dimension) --------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+          "l"(reinterpret_cast<uint64_t>(m)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_smem_to_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+}  // namespace sscan

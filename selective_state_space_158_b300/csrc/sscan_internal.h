@@ -1,0 +1,51 @@
+// sscan_internal.h -- interfaces between the C ABI layer (sscan_api.cu) and the kernel
+// launchers (sscan_kernels.cu). Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sscan {
+
+enum class Io { F32 = 0, BF16 = 1 };
+
+// Everything a launcher needs: caller pointers and sizes, already validated.
+struct FwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;       // nullable
+  const void* z;        // nullable
+  const float* bias;    // nullable
+  int softplus;
+  void* y;
+  float* h_last;        // nullable
+  int64_t batch, L, dim, N;
+  Io io;
+  cudaStream_t stream;
+  unsigned int* status;  // device status word (SSCAN_ERR_* bit set on device-side errors)
+};
+
+// Tuning knobs of the TMA-staged kernel. Zero fields mean "choose automatically".
+struct TmaTuning {
+  int states_per_lane = 0;    // K: states of one channel a lane holds (4, 8 or 16)
+  int segments = 0;           // time segments run by different CTAs (chunk carry)
+  int threads = 0;            // threads per CTA (multiple of 32, <= 256)
+  int stages = 0;             // TMA pipeline depth
+};
+
+// True if the TMA-staged kernel can serve these arguments (alignment and stride rules of TMA).
+bool tma_path_ok(const FwdArgs& a);
+
+// Launchers. Return cudaSuccess or the launch error.
+cudaError_t launch_simple(const FwdArgs& a);
+cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& t);
+cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& t);
+
+// Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS from the environment (0: unset).
+TmaTuning tuning_from_env();
+
+}  // namespace sscan

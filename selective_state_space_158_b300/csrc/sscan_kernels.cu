@@ -1,0 +1,704 @@
+// sscan_kernels.cu -- the selective-scan forward kernels for sm_103a and their launchers.
+//
+// The scan follows "Mamba：选择性状态空间模型入门教程" (selective-scan pseudo-code: B_t, C_t and
+// Delta_t from the input, h_t = discretize_A(Delta) h_{t-1} + discretize_B(Delta, B) x_t,
+// y_t = C h_t), with the zero-order-hold A of "架构变体：Mamba/SSM" ("离散化") and the fusion
+// principle of its "硬件感知算法" section: the N-wide state of every channel lives in registers
+// for the whole sequence and only inputs and outputs touch HBM.
+//
+// Two kernels:
+//   * sscan_tma_kernel: the fast path. A CTA owns CH consecutive channels of one batch row and
+//     walks the sequence in chunks of TC steps. One thread streams the chunk's u/delta/z tiles
+//     and B/C rows into shared memory with TMA (double-buffered, mbarrier-tracked); all threads
+//     then turn (delta, u) into (dt, dt*u) once per (step, channel); then every lane advances its
+//     share of the 16 states through the chunk with ex2 on the SFU and packed f32x2 FMAs, the
+//     lanes of one channel combine their partial readouts, and the gated result goes back to HBM
+//     through a TMA store.
+//   * sscan_simple_kernel: one thread per channel with plain loads; serves any alignment, any
+//     dim and any N <= 16.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <type_traits>
+
+#include <cudaTypedefs.h>
+
+#include "sscan_device.cuh"
+#include "sscan_internal.h"
+
+namespace sscan {
+
+constexpr int kNP = 16;          // states held per channel (N <= 16 is zero-padded to 16)
+constexpr uint32_t kWaitTries = 1u << 22;  // bound on one mbarrier wait (seconds, not forever)
+constexpr unsigned kErrTimeout = 1u << 4;  // status bit: a bounded wait ran out
+
+// ================================================================================================
+// Plain-load kernel: one thread per (batch row, channel), states in registers, sequential in t.
+// ================================================================================================
+template <typename IO>
+__global__ void __launch_bounds__(128) sscan_simple_kernel(
+    const IO* __restrict__ u, const IO* __restrict__ delta, const float* __restrict__ A,
+    const IO* __restrict__ Bm, const IO* __restrict__ Cm, const float* __restrict__ Dskip,
+    const IO* __restrict__ z, const float* __restrict__ bias, int softplus, IO* __restrict__ y,
+    float* __restrict__ h_last, int64_t batch, int64_t L, int64_t dim, int N) {
+  const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= batch * dim) return;
+  const int64_t b = c / dim, d = c - b * dim;
+  float A2[kNP], h[kNP];
+#pragma unroll
+  for (int n = 0; n < kNP; ++n) {
+    A2[n] = n < N ? A[d * N + n] * kLog2e : 0.f;
+    h[n] = 0.f;
+  }
+  const float bs = bias ? bias[d] : 0.f;
+  const float Dd = Dskip ? Dskip[d] : 0.f;
+  for (int64_t t = 0; t < L; ++t) {
+    const int64_t idx = (b * L + t) * dim + d;
+    const float x = to_f32(delta[idx]) + bs;
+    const float dt = softplus ? softplus_f(x) : x;
+    const float uu = to_f32(u[idx]);
+    const float dtu = dt * uu;
+    const IO* Bt = Bm + (b * L + t) * N;
+    const IO* Ct = Cm + (b * L + t) * N;
+    float acc = 0.f;
+#pragma unroll
+    for (int n = 0; n < kNP; ++n) {
+      if (n < N) {
+        const float e = ex2(fmaf(dt, A2[n], kEx2ArgShift));
+        h[n] = fmaf(e, h[n], dtu * to_f32(Bt[n]));
+        acc = fmaf(to_f32(Ct[n]), h[n], acc);
+      }
+    }
+    float yv = fmaf(Dd, uu, acc);
+    if (z) yv *= silu_f(to_f32(z[idx]));
+    store_io(y + idx, yv);
+  }
+  if (h_last) {
+#pragma unroll
+    for (int n = 0; n < kNP; ++n)
+      if (n < N) h_last[c * N + n] = h[n];
+  }
+}
+
+__host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
+
+// ================================================================================================
+// Lane-owned kernel. Every lane owns one channel's K = 16 / G states (G = 1 or 2 lanes per
+// channel); a warp owns 32 / G whole channels, and does its prologue (softplus), recurrence,
+// readout, skip, gate and y store for them without leaving registers. The CTA shares only the
+// TMA-staged input tiles and the B / C rows, widened once per chunk to fp32 and read by every
+// lane as broadcast 16-byte loads. One CTA barrier per chunk orders the widening.
+//
+// Long sequences are split into n_seg time segments run by different CTAs ("chunk carry"). The
+// scan operator (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) is associative ("架构变体：Mamba/SSM",
+// "硬件感知算法": the update can be evaluated as a tree), so a segment is summarised by its
+// aggregate: the end state from a zero start, H, and its summed step SD (its decay factor is
+// 2^(A log2e SD), exact for a product of zero-order-hold factors). A segment CTA
+//   1. runs pass 1 over its steps (no readout) to get (SD, H) and publishes it;
+//   2. looks back over its predecessors' published values (decoupled look-back): aggregates
+//      are composed until an inclusive prefix (the true end state of an earlier segment) is
+//      found, giving this segment's true start state h_in; it publishes its own inclusive;
+//   3. runs pass 2 from h_in with readout, gate and stores.
+// CTAs take segment numbers from an atomic ticket in launch order, segment-major, so every CTA
+// they wait on is already resident or finished; every wait is bounded and reports a timeout
+// through the device status word instead of hanging.
+// ================================================================================================
+struct LaneParams {
+  const float* A;
+  const float* D;
+  const float* bias;
+  float* h_last;
+  unsigned int* status;
+  int L, dim, N, batch;
+  int softplus, has_z;
+  int n_chunks;    // chunks covering L
+  int stages;      // TMA pipeline depth
+  int n_cg;        // CTAs (channel groups) per batch row
+  int n_seg;       // time segments (1: no chunk carry)
+  int seg_chunks;  // chunks per segment
+  // chunk-carry workspace (n_seg > 1)
+  unsigned int* ticket;  // zero at launch
+  unsigned int* flags;   // [n_seg][batch][n_cg][W] warp units
+  float* agg;            // [unit][lane][K + 1]: H then SD
+  float* incl;           // [unit][lane][K]
+  int skip_publish;      // test hook: this segment never publishes (-1: off)
+};
+
+constexpr unsigned kFlagAgg = 1, kFlagIncl = 2, kFlagInclErr = 3;
+constexpr unsigned kErrCarry = 1u << 5;         // status bit: a look-back wait ran out
+constexpr uint32_t kLookbackTries = 1u << 21;  // x ~0.5 us sleep: about a second
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+struct LaneSmem {
+  size_t tile_io, bc_io, stage, off_stage, off_bc, off_y, y_warp, off_bar, total;
+  __host__ __device__ LaneSmem(int TC, int W, int CPW, int N, int es, int stages) {
+    const int CH = W * CPW;
+    tile_io = align128(size_t(TC) * CH * es);
+    bc_io = align128(size_t(TC) * N * es);
+    stage = 3 * tile_io + 2 * bc_io;  // u, delta, z, B, C
+    off_stage = 0;
+    off_bc = size_t(stages) * stage;                       // [2][TC][2][16] fp32
+    y_warp = align128(size_t(TC) * CPW * es);               // one warp's y tile
+    off_y = off_bc + align128(size_t(2) * TC * 32 * sizeof(float));
+    off_bar = off_y + size_t(2) * W * y_warp;               // [2][W] y tiles
+    total = off_bar + 8 * 8 + 16;                           // mbarriers, ticket
+  }
+};
+
+template <typename IO, int G, int TC>
+__global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
+    const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
+    const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
+    const LaneParams p) {
+  constexpr int K = kNP / G;     // states per lane
+  constexpr int KP = K / 2;      // float2 state registers per lane (states n, n+1 packed)
+  constexpr int CPW = 32 / G;    // channels per warp
+  static_assert(G == 1 || G == 2, "G must be 1 or 2");
+  static_assert(TC % 2 == 0, "chunk must be even");
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int W = nthr >> 5, CH = W * CPW;
+  const int N = p.N, S = p.stages;
+  const LaneSmem lay(TC, W, CPW, N, int(sizeof(IO)), S);
+  float* bc0 = reinterpret_cast<float*>(smem + lay.off_bc);  // [2][TC][32]: B[0..15], C[0..15]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
+  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + lay.off_bar + 8 * 8);
+
+  // ---- which work this CTA does: channel group, batch row, time segment ----
+  int cgi, b, seg;
+  if (p.n_seg == 1) {
+    cgi = blockIdx.x;
+    b = blockIdx.y;
+    seg = 0;
+  } else {
+    if (tid == 0) *s_ticket = atomicAdd(p.ticket, 1u);
+    __syncthreads();
+    const unsigned t = *s_ticket;  // segment-major: every earlier segment got an earlier ticket
+    const unsigned per_seg = unsigned(p.batch) * unsigned(p.n_cg);
+    seg = int(t / per_seg);
+    b = int((t % per_seg) / unsigned(p.n_cg));
+    cgi = int(t % unsigned(p.n_cg));
+  }
+  const int ch0 = cgi * CH;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
+  const int nch = c_end - c_begin;
+  const int passes = p.n_seg > 1 ? 2 : 1;  // pass 1 (aggregate) only with chunk carry
+  const int n_loads = passes * nch;
+
+  auto stage_ptr = [&](int s, int which) -> unsigned char* {  // 0 u, 1 delta, 2 z, 3 B, 4 C
+    unsigned char* base = smem + lay.off_stage + size_t(s) * lay.stage;
+    return which < 3 ? base + size_t(which) * lay.tile_io
+                     : base + 3 * lay.tile_io + size_t(which - 3) * lay.bc_io;
+  };
+  const uint32_t tile_bytes = uint32_t(TC) * CH * sizeof(IO);
+  const uint32_t bc_bytes = uint32_t(TC) * N * sizeof(IO);
+  const uint32_t stage_bytes = (p.has_z ? 3u : 2u) * tile_bytes + 2u * bc_bytes;
+  // Load q (0 .. n_loads-1) brings chunk c_begin + q % nch into stage q % S.
+  auto issue_load = [&](int q) {
+    const int s = q % S;
+    const int t0 = (c_begin + q % nch) * TC;
+    mbar_arrive_expect_tx(&full[s], stage_bytes);
+    tma_load_3d(stage_ptr(s, 0), &tm_u, ch0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 1), &tm_dl, ch0, t0, b, &full[s]);
+    if (p.has_z) tma_load_3d(stage_ptr(s, 2), &tm_z, ch0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 3), &tm_B, 0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 4), &tm_C, 0, t0, b, &full[s]);
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_u);
+    tma_prefetch_desc(&tm_dl);
+    if (p.has_z) tma_prefetch_desc(&tm_z);
+    tma_prefetch_desc(&tm_B);
+    tma_prefetch_desc(&tm_C);
+    tma_prefetch_desc(&tm_y);
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int q = 0; q < S && q < n_loads; ++q) issue_load(q);
+
+  const int warp = tid >> 5, lane = tid & 31;
+  const int cl = warp * CPW + lane / G;  // channel within the CTA
+  const int g = lane % G;                // which half of the states (G == 2)
+  const int n0 = g * K;
+  const int cg = ch0 + cl;               // global channel
+  const bool live = cg < p.dim;
+  float2 A2[KP], h[KP];
+#pragma unroll
+  for (int r = 0; r < KP; ++r) {
+    const int n = n0 + 2 * r;
+    A2[r] = f2((live && n < N) ? p.A[size_t(cg) * N + n] * kLog2e : 0.f,
+               (live && n + 1 < N) ? p.A[size_t(cg) * N + n + 1] * kLog2e : 0.f);
+    h[r] = f2(0.f, 0.f);
+  }
+  const float bias_c = (p.bias && live) ? p.bias[cg] : 0.f;
+  const float D_c = (p.D && live) ? p.D[cg] : 0.f;
+  IO* ywarp0 = reinterpret_cast<IO*>(smem + lay.off_y) + size_t(warp) * (lay.y_warp / sizeof(IO));
+
+  bool timed_out = false;
+  float sd = 0.f, sd_c = 0.f;  // Kahan sum of this segment's steps (pass 1)
+  int q = 0;                   // loads consumed
+  int ystores = 0;             // y tiles this warp has stored
+  for (int pass = passes == 2 ? 0 : 1; pass < 2 && !timed_out; ++pass) {
+    const bool readout = pass == 1;
+    for (int ci = 0; ci < nch; ++ci, ++q) {
+      const int c = c_begin + ci;
+      const int s = q % S;
+      const int t0 = c * TC;
+      const int t_valid = min(TC, p.L - t0);
+      const bool landed = mbar_wait_bounded(&full[s], (q / S) & 1, kWaitTries);
+      const IO* B_s = reinterpret_cast<const IO*>(stage_ptr(s, 3));
+      const IO* C_s = reinterpret_cast<const IO*>(stage_ptr(s, 4));
+      float* bc = bc0 + (q & 1) * (TC * 32);
+      if (landed) {
+        for (int i = tid; i < TC * 32; i += nthr) {
+          const int t = i >> 5, k = i & 31, n = k & 15;
+          const IO* src = k < 16 ? B_s : C_s;
+          bc[i] = n < N ? to_f32(src[t * N + n]) : 0.f;
+        }
+      }
+      if (__syncthreads_or(!landed)) {  // CTA-uniform: every thread leaves together
+        timed_out = true;
+        break;
+      }
+      // Every warp has finished load q-1, so its stage can take load q-1+S.
+      if (tid == 0 && q >= 1 && q - 1 + S < n_loads) issue_load(q - 1 + S);
+
+      const IO* u_s = reinterpret_cast<const IO*>(stage_ptr(s, 0)) + cl;
+      const IO* dl_s = reinterpret_cast<const IO*>(stage_ptr(s, 1)) + cl;
+      const IO* z_s = reinterpret_cast<const IO*>(stage_ptr(s, 2)) + cl;
+
+      // Prologue, two steps at a time in f32x2: dt = softplus(delta + bias) and dt * u for
+      // every step of the chunk (both lanes of a channel compute it when G == 2). Steps past
+      // the end of the sequence get dt = 0, an identity update.
+      float dt[TC], dtu[TC], uk[TC];
+#pragma unroll
+      for (int k = 0; k < TC / 2; ++k) {
+        const int t = 2 * k;
+        const float2 u2 = f2(to_f32(u_s[t * CH]), to_f32(u_s[(t + 1) * CH]));
+        float2 d2 = __fadd2_rn(f2(to_f32(dl_s[t * CH]), to_f32(dl_s[(t + 1) * CH])),
+                               f2(bias_c, bias_c));
+        if (p.softplus) d2 = softplus2(d2);
+        d2 = f2(t < t_valid ? d2.x : 0.f, t + 1 < t_valid ? d2.y : 0.f);
+        const float2 du = __fmul2_rn(d2, u2);
+        dt[t] = d2.x;
+        dt[t + 1] = d2.y;
+        dtu[t] = du.x;
+        dtu[t + 1] = du.y;
+        uk[t] = u2.x;
+        uk[t + 1] = u2.y;
+      }
+
+      if (!readout) {
+        // Pass 1: state from a zero start, no readout; and the segment's summed step.
+        float csum = 0.f;
+#pragma unroll
+        for (int t = 0; t < TC; ++t) {
+          const float4* Bq = reinterpret_cast<const float4*>(bc + t * 32 + n0);
+          const float2 dt2 = f2(dt[t], dt[t]), dtu2 = f2(dtu[t], dtu[t]);
+          csum += dt[t];
+#pragma unroll
+          for (int qq = 0; qq < K / 4; ++qq) {
+            const float4 bq = Bq[qq];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int r = 2 * qq + j;
+              const float2 arg = __ffma2_rn(dt2, A2[r], f2(kEx2ArgShift, kEx2ArgShift));
+              const float2 dA = f2(ex2(arg.x), ex2(arg.y));
+              const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
+              h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtu2, bb));
+            }
+          }
+        }
+        const float yk = csum - sd_c;  // Kahan step
+        const float tk = sd + yk;
+        sd_c = (tk - sd) - yk;
+        sd = tk;
+        continue;
+      }
+
+      // Pass 2 (or the only pass): ZOH decay on the SFU, packed f32x2 FMAs for the state and
+      // the readout.
+      float ys[TC];
+#pragma unroll
+      for (int t = 0; t < TC; ++t) {
+        const float4* Bq = reinterpret_cast<const float4*>(bc + t * 32 + n0);
+        const float4* Cq = reinterpret_cast<const float4*>(bc + t * 32 + 16 + n0);
+        const float2 dt2 = f2(dt[t], dt[t]), dtu2 = f2(dtu[t], dtu[t]);
+        float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+#pragma unroll
+        for (int qq = 0; qq < K / 4; ++qq) {
+          const float4 bq = Bq[qq], cq = Cq[qq];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int r = 2 * qq + j;
+            const float2 arg = __ffma2_rn(dt2, A2[r], f2(kEx2ArgShift, kEx2ArgShift));
+            const float2 dA = f2(ex2(arg.x), ex2(arg.y));
+            const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
+            const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
+            h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtu2, bb));
+            if (j) acc1 = __ffma2_rn(cc, h[r], acc1);
+            else acc0 = __ffma2_rn(cc, h[r], acc0);
+          }
+        }
+        const float2 acc = __fadd2_rn(acc0, acc1);
+        ys[t] = acc.x + acc.y;
+      }
+
+      // Epilogue on this lane's own steps, two at a time: (readout + D u) * SiLU(z) into the
+      // warp's y tile. With G == 2 the partner lanes first trade partial readouts so that lane
+      // g holds the full readout of steps t + g.
+      if (lane == 0 && ystores >= 2) tma_store_wait_read<1>();  // tile of two stores ago read
+      __syncwarp();
+      IO* yw = ywarp0 + size_t(ystores & 1) * (size_t(W) * lay.y_warp / sizeof(IO));
+      constexpr int OWN = TC / G;
+      float yo[OWN], uo[OWN];
+#pragma unroll
+      for (int k = 0; k < OWN; ++k) {
+        if constexpr (G == 1) {
+          yo[k] = ys[k];
+          uo[k] = uk[k];
+        } else {
+          const int t = 2 * k;
+          const float send = g ? ys[t] : ys[t + 1], keep = g ? ys[t + 1] : ys[t];
+          yo[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+          uo[k] = g ? uk[t + 1] : uk[t];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < OWN; k += 2) {
+        const int ta = G * k + g, tb = G * (k + 1) + g;  // this lane's steps
+        float2 y2 = __ffma2_rn(f2(D_c, D_c), f2(uo[k], uo[k + 1]), f2(yo[k], yo[k + 1]));
+        if (p.has_z)
+          y2 = __fmul2_rn(y2, silu2(f2(to_f32(z_s[ta * CH]), to_f32(z_s[tb * CH]))));
+        store_io(yw + ta * CPW + lane / G, y2.x);
+        store_io(yw + tb * CPW + lane / G, y2.y);
+      }
+      fence_smem_to_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_y, yw, ch0 + warp * CPW, t0, b);
+        tma_store_commit();
+      }
+      ++ystores;
+    }
+    if (pass == 0 && !timed_out) {
+      // ---- chunk carry: publish this segment's aggregate, look back, publish inclusive ----
+      const size_t unit = ((size_t(seg) * p.batch + b) * p.n_cg + cgi) * W + warp;
+      const size_t units_per_seg = size_t(p.batch) * p.n_cg * W;
+      float* my_agg = p.agg + (unit * 32 + lane) * (K + 1);
+      float* my_incl = p.incl + (unit * 32 + lane) * K;
+      const bool publish = seg != p.skip_publish;
+      float2 Hs[KP];
+#pragma unroll
+      for (int r = 0; r < KP; ++r) Hs[r] = h[r];
+      const float sd_s = sd;
+      bool carry_err = false;
+      float2 hin[KP];
+      if (seg == 0) {
+#pragma unroll
+        for (int r = 0; r < KP; ++r) hin[r] = f2(0.f, 0.f);
+      } else {
+        if (publish) {
+#pragma unroll
+          for (int r = 0; r < KP; ++r) {
+            my_agg[2 * r] = Hs[r].x;
+            my_agg[2 * r + 1] = Hs[r].y;
+          }
+          my_agg[K] = sd_s;
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) st_release(p.flags + unit, kFlagAgg);
+        }
+        // Look back: compose predecessors' aggregates (earlier o later) until an inclusive.
+        float2 accH[KP];
+#pragma unroll
+        for (int r = 0; r < KP; ++r) accH[r] = f2(0.f, 0.f);
+        float acc_sd = 0.f;
+        for (int j = seg - 1; j >= 0; --j) {
+          const size_t uj = unit - size_t(seg - j) * units_per_seg;
+          unsigned f = 0;
+          if (lane == 0) {
+            for (uint32_t it = 0; it < kLookbackTries; ++it) {
+              f = ld_acquire(p.flags + uj);
+              if (f != 0) break;
+              __nanosleep(512);
+            }
+            if (f == 0) {
+              atomicOr(p.status, kErrCarry);
+              f = kFlagInclErr;
+            }
+          }
+          f = __shfl_sync(0xffffffffu, f, 0);
+          __syncwarp();
+          if (f == kFlagAgg) {
+            const float* a = p.agg + (uj * 32 + lane) * (K + 1);
+            const float sdj = __ldcg(a + K);
+#pragma unroll
+            for (int r = 0; r < KP; ++r) {  // acc <- agg_j o acc
+              const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+              accH[r] = __ffma2_rn(dec, f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
+            }
+            acc_sd += sdj;
+            continue;
+          }
+          carry_err = f == kFlagInclErr;
+          const float* ic = p.incl + (uj * 32 + lane) * K;
+#pragma unroll
+          for (int r = 0; r < KP; ++r) {  // h_in = incl_j o acc
+            const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+            hin[r] = __ffma2_rn(dec, f2(__ldcg(ic + 2 * r), __ldcg(ic + 2 * r + 1)), accH[r]);
+          }
+          break;
+        }
+      }
+      // Inclusive of this segment: its true end state = decay(sd_s) h_in + H_s.
+      if (publish) {
+#pragma unroll
+        for (int r = 0; r < KP; ++r) {
+          const float2 dec = f2(ex2(A2[r].x * sd_s), ex2(A2[r].y * sd_s));
+          const float2 e = __ffma2_rn(dec, hin[r], Hs[r]);
+          my_incl[2 * r] = e.x;
+          my_incl[2 * r + 1] = e.y;
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release(p.flags + unit, carry_err ? kFlagInclErr : kFlagIncl);
+      }
+#pragma unroll
+      for (int r = 0; r < KP; ++r) h[r] = hin[r];
+    }
+  }
+
+  if (timed_out) {
+    if (tid == 0) {
+      atomicOr(p.status, kErrTimeout);
+      for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 1024);
+    }
+  } else if (p.h_last && live && seg == p.n_seg - 1) {
+    float* dst = p.h_last + (size_t(b) * p.dim + cg) * N;
+#pragma unroll
+    for (int r = 0; r < KP; ++r) {
+      const int n = n0 + 2 * r;
+      if (n < N) dst[n] = h[r].x;
+      if (n + 1 < N) dst[n + 1] = h[r].y;
+    }
+  }
+  if (lane == 0) tma_store_wait_all();
+}
+
+// ================================================================================================
+// Host side.
+// ================================================================================================
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t b0, uint32_t b1) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const uint64_t es = io == Io::F32 ? 4 : 2;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, io == Io::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+int env_int_or(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : dflt;
+}
+
+constexpr int kLaneTC = 16;
+
+template <typename IO, int G>
+cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
+  constexpr int CPW = 32 / G;
+  constexpr int K = kNP / G;
+  const int W = threads / 32;
+  const int CH = W * CPW;
+  LaneParams p;
+  p.A = a.A;
+  p.D = a.D;
+  p.bias = a.bias;
+  p.h_last = a.h_last;
+  p.status = a.status;
+  p.L = int(a.L);
+  p.dim = int(a.dim);
+  p.N = int(a.N);
+  p.batch = int(a.batch);
+  p.softplus = a.softplus;
+  p.has_z = a.z != nullptr;
+  p.n_chunks = int((a.L + kLaneTC - 1) / kLaneTC);
+  p.n_cg = int((a.dim + CH - 1) / CH);
+  // Chunk carry: split the sequence when too few warps would run otherwise (about 2 per SM).
+  const int64_t warps_per_seg = a.batch * p.n_cg * W;
+  int n_seg = segments;
+  if (n_seg <= 0) {
+    n_seg = 1;
+    if (warps_per_seg < 300) n_seg = int((148 * 8 + warps_per_seg - 1) / warps_per_seg);
+  }
+  n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
+  p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
+  n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;  // no empty segments
+  p.n_seg = n_seg;
+  p.skip_publish = env_int_or("SSCAN_TEST_SKIP_PUBLISH", -1);
+  const int es = a.io == Io::F32 ? 4 : 2;
+  if (stages < 2 || stages > 8) stages = 3;
+  while (stages > 2 &&
+         LaneSmem(kLaneTC, W, CPW, int(a.N), es, stages).total + 128 > size_t(227) * 1024)
+    --stages;
+  p.stages = stages;
+  const LaneSmem lay(kLaneTC, W, CPW, int(a.N), es, stages);
+  const size_t smem_bytes = lay.total + 128;
+  if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
+  CUtensorMap mu, md, mz, mB, mC, my;
+  const uint64_t dim = a.dim, L = a.L, bt = a.batch, N = a.N;
+  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&md, a.delta, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&mB, a.B, a.io, N, L, bt, uint32_t(N), kLaneTC) &&
+            make_map(&mC, a.C, a.io, N, L, bt, uint32_t(N), kLaneTC) &&
+            make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = sscan_lane_kernel<IO, G, kLaneTC>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
+  if (e != cudaSuccess) return e;
+  void* ws = nullptr;
+  if (n_seg > 1) {
+    // Stream-ordered workspace: ticket, flags, aggregates, inclusive prefixes.
+    const size_t units = size_t(n_seg) * warps_per_seg;
+    const size_t flag_bytes = align128(sizeof(unsigned) * (1 + units));
+    const size_t bytes = flag_bytes + units * 32 * (2 * K + 1) * sizeof(float);
+    e = cudaMallocAsync(&ws, bytes, a.stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(ws, 0, flag_bytes, a.stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ws, a.stream);
+      return e;
+    }
+    p.ticket = static_cast<unsigned*>(ws);
+    p.flags = p.ticket + 1;
+    p.agg = reinterpret_cast<float*>(static_cast<char*>(ws) + flag_bytes);
+    p.incl = p.agg + units * 32 * (K + 1);
+  } else {
+    p.ticket = p.flags = nullptr;
+    p.agg = p.incl = nullptr;
+  }
+  if (n_seg > 1) {
+    kern<<<unsigned(n_seg * warps_per_seg / W), threads, smem_bytes, a.stream>>>(mu, md, mz, mB,
+                                                                                 mC, my, p);
+  } else {
+    dim3 grid(unsigned(p.n_cg), unsigned(bt), 1);
+    kern<<<grid, threads, smem_bytes, a.stream>>>(mu, md, mz, mB, mC, my, p);
+  }
+  e = cudaGetLastError();
+  if (ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, a.stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
+  int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
+  if (G == 0) {
+    const int64_t chans = a.batch * a.dim;
+    G = chans >= 148 * 128 ? 1 : 2;
+  }
+  const int threads = tune.threads ? tune.threads : 64;
+  if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
+  const int es = a.io == Io::F32 ? 4 : 2;
+  if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
+  if (a.io == Io::F32)
+    return G == 1 ? launch_lane_typed<float, 1>(a, threads, tune.stages, tune.segments)
+                  : launch_lane_typed<float, 2>(a, threads, tune.stages, tune.segments);
+  return G == 1 ? launch_lane_typed<__nv_bfloat16, 1>(a, threads, tune.stages, tune.segments)
+                : launch_lane_typed<__nv_bfloat16, 2>(a, threads, tune.stages, tune.segments);
+}
+
+TmaTuning tuning_from_env() {
+  TmaTuning t;
+  t.states_per_lane = env_int("SSCAN_K");
+  t.segments = env_int("SSCAN_SEGMENTS");
+  t.threads = env_int("SSCAN_THREADS");
+  t.stages = env_int("SSCAN_STAGES");
+  return t;
+}
+
+bool tma_path_ok(const FwdArgs& a) {
+  const int64_t es = a.io == Io::F32 ? 4 : 2;
+  if (!aligned16(a.u) || !aligned16(a.delta) || !aligned16(a.B) || !aligned16(a.C) ||
+      !aligned16(a.y) || (a.z && !aligned16(a.z)))
+    return false;
+  if ((a.dim * es) % 16 != 0 || (a.N * es) % 16 != 0) return false;
+  if (a.L > INT32_MAX - 64 || a.dim > INT32_MAX || a.batch > 65535) return false;
+  return get_encode() != nullptr;
+}
+
+cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& tune) { return launch_lane(a, tune); }
+
+cudaError_t launch_simple(const FwdArgs& a) {
+  const int64_t chans = a.batch * a.dim;
+  const int threads = 128;
+  const unsigned blocks = unsigned((chans + threads - 1) / threads);
+  if (a.io == Io::F32) {
+    sscan_simple_kernel<float><<<blocks, threads, 0, a.stream>>>(
+        static_cast<const float*>(a.u), static_cast<const float*>(a.delta), a.A,
+        static_cast<const float*>(a.B), static_cast<const float*>(a.C), a.D,
+        static_cast<const float*>(a.z), a.bias, a.softplus, static_cast<float*>(a.y), a.h_last,
+        a.batch, a.L, a.dim, int(a.N));
+  } else {
+    using bf = __nv_bfloat16;
+    sscan_simple_kernel<bf><<<blocks, threads, 0, a.stream>>>(
+        static_cast<const bf*>(a.u), static_cast<const bf*>(a.delta), a.A,
+        static_cast<const bf*>(a.B), static_cast<const bf*>(a.C), a.D,
+        static_cast<const bf*>(a.z), a.bias, a.softplus, static_cast<bf*>(a.y), a.h_last,
+        a.batch, a.L, a.dim, int(a.N));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sscan

@@ -1,0 +1,58 @@
+"""The C ABI library loads without a GPU and exports every symbol include/sscan.h declares;
+argument errors come back synchronously, before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_158_b300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[\w\s\*]+?\b(sscan_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = declared_functions()
+    assert {"sscan_fwd", "sscan_fwd_host", "sscan_get_device_error", "sscan_status_string",
+            "sscan_release"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+        assert n in binding.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "SSCAN_OK"
+    assert binding.status_string(4) == "SSCAN_ERR_CARRY_TIMEOUT"
+    assert binding.status_string(99) == "SSCAN_ERR_UNKNOWN"
+
+
+def test_argument_errors_are_synchronous_without_a_device(lib):
+    dummy = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
+    ok = [dummy, dummy, dummy, dummy, dummy, None, None, None, 1, dummy, None, 1, 8, 64, 16, 0,
+          None]
+    for idx, val in [(14, 0), (14, 17), (12, -1), (11, -2), (13, -1), (15, 3), (0, None),
+                     (2, None), (9, None), (3, None)]:
+        args = list(ok)
+        args[idx] = val
+        assert lib.sscan_fwd(*args) == 1, (idx, val)
+        assert lib.sscan_fwd_host(*args) == 1, (idx, val)
+    # size products that overflow int64
+    args = list(ok)
+    args[11], args[12], args[13] = 1 << 40, 1 << 40, 64
+    assert lib.sscan_fwd(*args) == 1
