@@ -33,7 +33,7 @@ typedef enum {
   SSCAN_ERR_INVALID_ARG = 1,   /* null required pointer, negative size, N outside 1..16, ... */
   SSCAN_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (no such case today) */
   SSCAN_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
-  SSCAN_ERR_CARRY_TIMEOUT = 4  /* device side: a chunk-carry wait ran out of its bound */
+  SSCAN_ERR_CARRY_TIMEOUT = 4  /* device side: a bounded wait (pipeline or chunk carry) ran out */
 } sscan_status_t;
 
 /*
@@ -81,7 +81,8 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
                               sscan_dtype_t dtype, cudaStream_t stream);
 
 /* Synchronizes `stream`, then reads and clears the current device's status word (set by
- * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT). Returns SSCAN_OK if clear. */
+ * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT). Allocates nothing.
+ * Returns SSCAN_OK if clear. */
 sscan_status_t sscan_get_device_error(cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -47,10 +47,14 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
   return true;
 }
 
+}  // namespace
+
+namespace sscan {
+
 // Shared validation of sizes and pointer presence; fills the element counts.
-sscan_status_t check_args(const void* u, const void* delta, const float* A, const void* B,
-                          const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
-                          int64_t N, sscan_dtype_t dtype, int64_t* n_bld, int64_t* n_bln) {
+int check_fwd_args(const void* u, const void* delta, const float* A, const void* B,
+                   const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
+                   int64_t N, int dtype, int64_t* n_bld, int64_t* n_bln) {
   if (dtype != SSCAN_F32 && dtype != SSCAN_BF16) return SSCAN_ERR_INVALID_ARG;
   if (batch < 0 || L < 0 || dim < 0 || N < 1 || N > 16) return SSCAN_ERR_INVALID_ARG;
   int64_t bl, bld, bln, bd, bdn, bytes;
@@ -63,6 +67,17 @@ sscan_status_t check_args(const void* u, const void* delta, const float* A, cons
   if (bd == 0 || L == 0) return SSCAN_OK;  // nothing to read
   if (!A || !u || !delta || !B || !C || !y) return SSCAN_ERR_INVALID_ARG;
   return SSCAN_OK;
+}
+
+}  // namespace sscan
+
+namespace {
+
+sscan_status_t check_args(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
+                          int64_t N, sscan_dtype_t dtype, int64_t* n_bld, int64_t* n_bln) {
+  return static_cast<sscan_status_t>(
+      sscan::check_fwd_args(u, delta, A, B, C, y, batch, L, dim, N, int(dtype), n_bld, n_bln));
 }
 
 }  // namespace
@@ -197,10 +212,14 @@ sscan_status_t sscan_get_device_error(cudaStream_t stream) {
   const int dev = current_device();
   if (dev < 0) return SSCAN_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SSCAN_ERR_CUDA;
-  unsigned int* w = status_word(dev);
-  if (!w) return SSCAN_ERR_CUDA;
+  unsigned int* w = nullptr;  // sscan_fwd's word, if any call created it (no allocation here)
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    w = g_dev[dev].status;
+  }
   unsigned int v = 0;
-  if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SSCAN_ERR_CUDA;
+  if (w && cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SSCAN_ERR_CUDA;
   if (v == 0) return SSCAN_OK;
   if (cudaMemset(w, 0, sizeof v) != cudaSuccess) return SSCAN_ERR_CUDA;
   return SSCAN_ERR_CARRY_TIMEOUT;

@@ -37,6 +37,11 @@ struct TmaTuning {
   int stages = 0;             // TMA pipeline depth
 };
 
+// Size checks shared by the C entry points; fills the element counts (batch*L*dim, batch*L*N).
+int check_fwd_args(const void* u, const void* delta, const float* A, const void* B,
+                   const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
+                   int64_t N, int dtype, int64_t* n_bld, int64_t* n_bln);
+
 // True if the TMA-staged kernel can serve these arguments (alignment and stride rules of TMA).
 bool tma_path_ok(const FwdArgs& a);
 

@@ -95,14 +95,15 @@ __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_
 // "硬件感知算法": the update can be evaluated as a tree), so a segment is summarised by its
 // aggregate: the end state from a zero start, H, and its summed step SD (its decay factor is
 // 2^(A log2e SD), exact for a product of zero-order-hold factors). A segment CTA
-//   1. runs pass 1 over its steps (no readout) to get (SD, H) and publishes it;
-//   2. looks back over its predecessors' published values (decoupled look-back): aggregates
-//      are composed until an inclusive prefix (the true end state of an earlier segment) is
-//      found, giving this segment's true start state h_in; it publishes its own inclusive;
+//   1. runs pass 1 over its steps (no readout) and publishes its aggregate (if it has a
+//      successor);
+//   2. looks back over every predecessor's published aggregate and folds them, nearest first,
+//      into its true start state h_in (a fixed order: the result is deterministic);
 //   3. runs pass 2 from h_in with readout, gate and stores.
-// CTAs take segment numbers from an atomic ticket in launch order, segment-major, so every CTA
-// they wait on is already resident or finished; every wait is bounded and reports a timeout
-// through the device status word instead of hanging.
+// Aggregates depend on nothing but the segment's own inputs, so no wait forms a chain. CTAs take
+// segment numbers from an atomic ticket in launch order, segment-major, so every CTA they wait
+// on is already resident or finished; every wait is bounded and reports a timeout through the
+// device status word instead of hanging.
 // ================================================================================================
 struct LaneParams {
   const float* A;
@@ -121,11 +122,10 @@ struct LaneParams {
   unsigned int* ticket;  // zero at launch
   unsigned int* flags;   // [n_seg][batch][n_cg][W] warp units
   float* agg;            // [unit][lane][K + 1]: H then SD
-  float* incl;           // [unit][lane][K]
   int skip_publish;      // test hook: this segment never publishes (-1: off)
 };
 
-constexpr unsigned kFlagAgg = 1, kFlagIncl = 2, kFlagInclErr = 3;
+constexpr unsigned kFlagAgg = 1;
 constexpr unsigned kErrCarry = 1u << 5;         // status bit: a look-back wait ran out
 constexpr uint32_t kLookbackTries = 1u << 21;  // x ~0.5 us sleep: about a second
 
@@ -195,7 +195,9 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   const int c_begin = seg * p.seg_chunks;
   const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
   const int nch = c_end - c_begin;
-  const int passes = p.n_seg > 1 ? 2 : 1;  // pass 1 (aggregate) only with chunk carry
+  // Pass 1 (aggregate only) runs for every segment that has a successor.
+  const bool agg_pass = p.n_seg > 1 && seg + 1 < p.n_seg;
+  const int passes = agg_pass ? 2 : 1;
   const int n_loads = passes * nch;
 
   auto stage_ptr = [&](int s, int which) -> unsigned char* {  // 0 u, 1 delta, 2 z, 3 B, 4 C
@@ -253,8 +255,43 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   float sd = 0.f, sd_c = 0.f;  // Kahan sum of this segment's steps (pass 1)
   int q = 0;                   // loads consumed
   int ystores = 0;             // y tiles this warp has stored
-  for (int pass = passes == 2 ? 0 : 1; pass < 2 && !timed_out; ++pass) {
+  const size_t unit = ((size_t(seg) * p.batch + b) * p.n_cg + cgi) * W + warp;
+  const size_t units_per_seg = size_t(p.batch) * p.n_cg * W;
+  for (int pass = agg_pass ? 0 : 1; pass < 2 && !timed_out; ++pass) {
     const bool readout = pass == 1;
+    if (readout && p.n_seg > 1) {
+      // Start state of this segment: predecessors' aggregates folded from the nearest back to
+      // segment 0 (later o earlier), always in that order, so the result is deterministic.
+      // (Segment 0 starts from zero; pass 1 left its aggregate in h.)
+      float2 accH[KP];
+#pragma unroll
+      for (int r = 0; r < KP; ++r) accH[r] = f2(0.f, 0.f);
+      float acc_sd = 0.f;
+      for (int j = seg - 1; j >= 0; --j) {
+        const size_t uj = unit - size_t(seg - j) * units_per_seg;
+        unsigned f = 0;
+        if (lane == 0) {
+          for (uint32_t it = 0; it < kLookbackTries; ++it) {
+            f = ld_acquire(p.flags + uj);
+            if (f != 0) break;
+            __nanosleep(512);
+          }
+          if (f == 0) atomicOr(p.status, kErrCarry);
+        }
+        f = __shfl_sync(0xffffffffu, f, 0);
+        __syncwarp();
+        if (f == 0) continue;  // timed out: the status word says so; skip this aggregate
+        const float* a = p.agg + (uj * 32 + lane) * (K + 1);
+#pragma unroll
+        for (int r = 0; r < KP; ++r) {  // acc <- acc o agg_j: agg_j's end state decays over acc
+          const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+          accH[r] = __ffma2_rn(dec, f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
+        }
+        acc_sd += __ldcg(a + K);
+      }
+#pragma unroll
+      for (int r = 0; r < KP; ++r) h[r] = accH[r];
+    }
     for (int ci = 0; ci < nch; ++ci, ++q) {
       const int c = c_begin + ci;
       const int s = q % S;
@@ -396,91 +433,18 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       }
       ++ystores;
     }
-    if (pass == 0 && !timed_out) {
-      // ---- chunk carry: publish this segment's aggregate, look back, publish inclusive ----
-      const size_t unit = ((size_t(seg) * p.batch + b) * p.n_cg + cgi) * W + warp;
-      const size_t units_per_seg = size_t(p.batch) * p.n_cg * W;
+    if (pass == 0 && !timed_out && seg != p.skip_publish) {
+      // Publish this segment's aggregate: end state from a zero start, and its summed step.
       float* my_agg = p.agg + (unit * 32 + lane) * (K + 1);
-      float* my_incl = p.incl + (unit * 32 + lane) * K;
-      const bool publish = seg != p.skip_publish;
-      float2 Hs[KP];
 #pragma unroll
-      for (int r = 0; r < KP; ++r) Hs[r] = h[r];
-      const float sd_s = sd;
-      bool carry_err = false;
-      float2 hin[KP];
-      if (seg == 0) {
-#pragma unroll
-        for (int r = 0; r < KP; ++r) hin[r] = f2(0.f, 0.f);
-      } else {
-        if (publish) {
-#pragma unroll
-          for (int r = 0; r < KP; ++r) {
-            my_agg[2 * r] = Hs[r].x;
-            my_agg[2 * r + 1] = Hs[r].y;
-          }
-          my_agg[K] = sd_s;
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release(p.flags + unit, kFlagAgg);
-        }
-        // Look back: compose predecessors' aggregates (earlier o later) until an inclusive.
-        float2 accH[KP];
-#pragma unroll
-        for (int r = 0; r < KP; ++r) accH[r] = f2(0.f, 0.f);
-        float acc_sd = 0.f;
-        for (int j = seg - 1; j >= 0; --j) {
-          const size_t uj = unit - size_t(seg - j) * units_per_seg;
-          unsigned f = 0;
-          if (lane == 0) {
-            for (uint32_t it = 0; it < kLookbackTries; ++it) {
-              f = ld_acquire(p.flags + uj);
-              if (f != 0) break;
-              __nanosleep(512);
-            }
-            if (f == 0) {
-              atomicOr(p.status, kErrCarry);
-              f = kFlagInclErr;
-            }
-          }
-          f = __shfl_sync(0xffffffffu, f, 0);
-          __syncwarp();
-          if (f == kFlagAgg) {
-            const float* a = p.agg + (uj * 32 + lane) * (K + 1);
-            const float sdj = __ldcg(a + K);
-#pragma unroll
-            for (int r = 0; r < KP; ++r) {  // acc <- agg_j o acc
-              const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
-              accH[r] = __ffma2_rn(dec, f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
-            }
-            acc_sd += sdj;
-            continue;
-          }
-          carry_err = f == kFlagInclErr;
-          const float* ic = p.incl + (uj * 32 + lane) * K;
-#pragma unroll
-          for (int r = 0; r < KP; ++r) {  // h_in = incl_j o acc
-            const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
-            hin[r] = __ffma2_rn(dec, f2(__ldcg(ic + 2 * r), __ldcg(ic + 2 * r + 1)), accH[r]);
-          }
-          break;
-        }
+      for (int r = 0; r < KP; ++r) {
+        my_agg[2 * r] = h[r].x;
+        my_agg[2 * r + 1] = h[r].y;
       }
-      // Inclusive of this segment: its true end state = decay(sd_s) h_in + H_s.
-      if (publish) {
-#pragma unroll
-        for (int r = 0; r < KP; ++r) {
-          const float2 dec = f2(ex2(A2[r].x * sd_s), ex2(A2[r].y * sd_s));
-          const float2 e = __ffma2_rn(dec, hin[r], Hs[r]);
-          my_incl[2 * r] = e.x;
-          my_incl[2 * r + 1] = e.y;
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release(p.flags + unit, carry_err ? kFlagInclErr : kFlagIncl);
-      }
-#pragma unroll
-      for (int r = 0; r < KP; ++r) h[r] = hin[r];
+      my_agg[K] = sd;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release(p.flags + unit, kFlagAgg);
     }
   }
 
@@ -575,7 +539,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   int n_seg = segments;
   if (n_seg <= 0) {
     n_seg = 1;
-    if (warps_per_seg < 300) n_seg = int((148 * 8 + warps_per_seg - 1) / warps_per_seg);
+    if (warps_per_seg < 300) n_seg = int((148 * 16 + warps_per_seg - 1) / warps_per_seg);
   }
   n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
   p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
@@ -605,25 +569,25 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return e;
   void* ws = nullptr;
+  const bool own_ws = true;
   if (n_seg > 1) {
-    // Stream-ordered workspace: ticket, flags, aggregates, inclusive prefixes.
+    // Workspace: ticket, flags, aggregates. Stream-ordered allocation.
     const size_t units = size_t(n_seg) * warps_per_seg;
     const size_t flag_bytes = align128(sizeof(unsigned) * (1 + units));
-    const size_t bytes = flag_bytes + units * 32 * (2 * K + 1) * sizeof(float);
+    const size_t bytes = flag_bytes + units * 32 * (K + 1) * sizeof(float);
     e = cudaMallocAsync(&ws, bytes, a.stream);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(ws, 0, flag_bytes, a.stream);
     if (e != cudaSuccess) {
-      cudaFreeAsync(ws, a.stream);
+      if (own_ws) cudaFreeAsync(ws, a.stream);
       return e;
     }
     p.ticket = static_cast<unsigned*>(ws);
     p.flags = p.ticket + 1;
     p.agg = reinterpret_cast<float*>(static_cast<char*>(ws) + flag_bytes);
-    p.incl = p.agg + units * 32 * (K + 1);
   } else {
     p.ticket = p.flags = nullptr;
-    p.agg = p.incl = nullptr;
+    p.agg = nullptr;
   }
   if (n_seg > 1) {
     kern<<<unsigned(n_seg * warps_per_seg / W), threads, smem_bytes, a.stream>>>(mu, md, mz, mB,
@@ -633,7 +597,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
     kern<<<grid, threads, smem_bytes, a.stream>>>(mu, md, mz, mB, mC, my, p);
   }
   e = cudaGetLastError();
-  if (ws) {
+  if (ws && own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, a.stream);
     if (e == cudaSuccess) e = e2;
   }
@@ -643,14 +607,19 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
 }  // namespace
 
 cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
+  // One lane per channel (16 states) when there are enough channels to fill the SMs, else two
+  // lanes per channel; when even that leaves fewer than about two warps per SM the sequence is
+  // split into time segments (chunk carry) and one lane per channel is used again.
+  const int threads = tune.threads ? tune.threads : 128;
+  if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
+  const int64_t chans = a.batch * a.dim;
   int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
   if (G == 0) {
-    const int64_t chans = a.batch * a.dim;
     G = chans >= 148 * 128 ? 1 : 2;
+    if (chans * 2 / 32 < 300) G = 1;  // time segments will supply the parallelism
   }
-  const int threads = tune.threads ? tune.threads : 64;
-  if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
+  if (G != 1 && G != 2) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
   if (a.io == Io::F32)
     return G == 1 ? launch_lane_typed<float, 1>(a, threads, tune.stages, tune.segments)
