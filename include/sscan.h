@@ -33,7 +33,9 @@ typedef enum {
   SSCAN_ERR_INVALID_ARG = 1,   /* null required pointer, negative size, N outside 1..16, ... */
   SSCAN_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (no such case today) */
   SSCAN_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
-  SSCAN_ERR_CARRY_TIMEOUT = 4  /* device side: a bounded wait (pipeline or chunk carry) ran out */
+  SSCAN_ERR_CARRY_TIMEOUT = 4, /* device side: a bounded wait (pipeline or chunk carry) ran out */
+  SSCAN_ERR_SCRATCH_TOO_SMALL = 5 /* sscan_fwd_noalloc: the call needs more scratch than the
+                                     library's fixed buffer holds */
 } sscan_status_t;
 
 /*
@@ -80,9 +82,40 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
                               int64_t batch, int64_t L, int64_t dim, int64_t N,
                               sscan_dtype_t dtype, cudaStream_t stream);
 
-/* Synchronizes `stream`, then reads and clears the current device's status word (set by
- * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT). Allocates nothing.
- * Returns SSCAN_OK if clear. */
+/*
+ * sscan_fwd_noalloc -- sscan_fwd for callers that must not allocate device memory.
+ *
+ * This entry point has no counterpart in the pages; it exists for callers that cannot call
+ * cudaMalloc (or cudaMallocAsync) at the point where they run the scan: code that runs while a
+ * caching allocator or a framework owns all device memory, real-time paths that cannot afford an
+ * allocation's possible synchronisation, or code whose memory budget is fixed up front.
+ *
+ * Arguments, layouts, results and errors are those of sscan_fwd; inputs and outputs are still
+ * the caller's device buffers. The only difference is the chunk-carry scratch used when a long
+ * sequence is split across thread blocks: instead of a stream-ordered allocation it lives in a
+ * fixed 16 MiB array in device memory that every GPU which loads the library keeps until the
+ * process exits. A call that would need more scratch than that (very long sequences with many
+ * channels) returns SSCAN_ERR_SCRATCH_TOO_SMALL before launching anything; sscan_fwd serves it.
+ *
+ * - The first call on a device looks up that device's copy of the array (with the device
+ *   current); make that first call before any stream capture.
+ * - All calls share the array and it keeps the last call's contents; each call clears the parts
+ *   that must start at zero on `stream`. Calls whose kernels overlap on the GPU (on different
+ *   streams, or from different host threads) race on the array: serialise them.
+ * - Device-side timeouts are recorded in a status word inside the array;
+ *   sscan_get_device_error (which allocates nothing either) reports and clears it together
+ *   with sscan_fwd's.
+ * - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+sscan_status_t sscan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                                 const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int softplus_flag, void* y,
+                                 float* h_last, int64_t batch, int64_t L, int64_t dim,
+                                 int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the current device's status words (set by
+ * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT, by sscan_fwd or
+ * sscan_fwd_noalloc calls). Allocates nothing. Returns SSCAN_OK if clear. */
 sscan_status_t sscan_get_device_error(cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libsscan.so")
 
 SSCAN_F32, SSCAN_BF16 = 0, 1
 STATUS = {0: "SSCAN_OK", 1: "SSCAN_ERR_INVALID_ARG", 2: "SSCAN_ERR_UNSUPPORTED",
-          3: "SSCAN_ERR_CUDA", 4: "SSCAN_ERR_CARRY_TIMEOUT"}
+          3: "SSCAN_ERR_CUDA", 4: "SSCAN_ERR_CARRY_TIMEOUT", 5: "SSCAN_ERR_SCRATCH_TOO_SMALL"}
 
 # Every symbol include/sscan.h declares, with its ctypes signature.
 _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -27,6 +27,7 @@ _FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i64,
 SIGNATURES = {
     "sscan_fwd": (_FWD_ARGS, _int),
     "sscan_fwd_host": (_FWD_ARGS, _int),
+    "sscan_fwd_noalloc": (_FWD_ARGS, _int),
     "sscan_get_device_error": ([_vp], _int),
     "sscan_status_string": ([_int], ctypes.c_char_p),
     "sscan_release": ([], _int),

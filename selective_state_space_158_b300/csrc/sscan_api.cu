@@ -91,6 +91,7 @@ const char* sscan_status_string(sscan_status_t s) {
     case SSCAN_ERR_UNSUPPORTED: return "SSCAN_ERR_UNSUPPORTED";
     case SSCAN_ERR_CUDA: return "SSCAN_ERR_CUDA";
     case SSCAN_ERR_CARRY_TIMEOUT: return "SSCAN_ERR_CARRY_TIMEOUT";
+    case SSCAN_ERR_SCRATCH_TOO_SMALL: return "SSCAN_ERR_SCRATCH_TOO_SMALL";
   }
   return "SSCAN_ERR_UNKNOWN";
 }
@@ -217,11 +218,16 @@ sscan_status_t sscan_get_device_error(cudaStream_t stream) {
     std::lock_guard<std::mutex> lk(g_mu);
     w = g_dev[dev].status;
   }
-  unsigned int v = 0;
+  unsigned int v = 0, v2 = 0;
   if (w && cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
     return SSCAN_ERR_CUDA;
-  if (v == 0) return SSCAN_OK;
-  if (cudaMemset(w, 0, sizeof v) != cudaSuccess) return SSCAN_ERR_CUDA;
+  // Calls of the allocation-free entry point record device errors in its own static word.
+  unsigned int* w2 = sscan::noalloc_status_word(dev);
+  if (w2 && cudaMemcpy(&v2, w2, sizeof v2, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SSCAN_ERR_CUDA;
+  if ((v | v2) == 0) return SSCAN_OK;
+  if (v && cudaMemset(w, 0, sizeof v) != cudaSuccess) return SSCAN_ERR_CUDA;
+  if (v2 && cudaMemset(w2, 0, sizeof v2) != cudaSuccess) return SSCAN_ERR_CUDA;
   return SSCAN_ERR_CARRY_TIMEOUT;
 }
 

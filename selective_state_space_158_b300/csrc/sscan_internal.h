@@ -27,6 +27,12 @@ struct FwdArgs {
   Io io;
   cudaStream_t stream;
   unsigned int* status;  // device status word (SSCAN_ERR_* bit set on device-side errors)
+  // Optional caller-provided chunk-carry scratch. When null the launcher takes stream-ordered
+  // scratch with cudaMallocAsync; when set it uses this buffer and allocates nothing, failing
+  // with *scratch_short = true if the launch would need more than scratch_bytes.
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  bool* scratch_short = nullptr;
 };
 
 // Tuning knobs of the TMA-staged kernel. Zero fields mean "choose automatically".
@@ -41,6 +47,9 @@ struct TmaTuning {
 int check_fwd_args(const void* u, const void* delta, const float* A, const void* B,
                    const void* C, const void* y, int64_t batch, int64_t L, int64_t dim,
                    int64_t N, int dtype, int64_t* n_bld, int64_t* n_bln);
+
+// Status word of the allocation-free entry point on device `dev` (null before its first call).
+unsigned int* noalloc_status_word(int dev);
 
 // True if the TMA-staged kernel can serve these arguments (alignment and stride rules of TMA).
 bool tma_path_ok(const FwdArgs& a);

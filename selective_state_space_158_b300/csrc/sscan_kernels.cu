@@ -569,14 +569,23 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return e;
   void* ws = nullptr;
-  const bool own_ws = true;
+  const bool own_ws = a.scratch == nullptr;
   if (n_seg > 1) {
-    // Workspace: ticket, flags, aggregates. Stream-ordered allocation.
+    // Workspace: ticket, flags, aggregates. Stream-ordered allocation, or the caller's fixed
+    // scratch.
     const size_t units = size_t(n_seg) * warps_per_seg;
     const size_t flag_bytes = align128(sizeof(unsigned) * (1 + units));
     const size_t bytes = flag_bytes + units * 32 * (K + 1) * sizeof(float);
-    e = cudaMallocAsync(&ws, bytes, a.stream);
-    if (e != cudaSuccess) return e;
+    if (own_ws) {
+      e = cudaMallocAsync(&ws, bytes, a.stream);
+      if (e != cudaSuccess) return e;
+    } else {
+      if (bytes > a.scratch_bytes) {
+        if (a.scratch_short) *a.scratch_short = true;
+        return cudaErrorInvalidValue;
+      }
+      ws = a.scratch;
+    }
     e = cudaMemsetAsync(ws, 0, flag_bytes, a.stream);
     if (e != cudaSuccess) {
       if (own_ws) cudaFreeAsync(ws, a.stream);
