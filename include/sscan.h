@@ -53,15 +53,17 @@ typedef enum {
  * softplus_flag != 0 applies softplus to delta + bias; 0 uses delta + bias as the step.
  * Sizes: batch, L, dim >= 0; 1 <= N <= 16. batch, L or dim = 0 is a no-op that returns
  * SSCAN_OK (h_last, if given, is zeroed when L = 0).
- * Any alignment and any dim are accepted; 16-byte aligned pointers with dim and N multiples of
- * 4 (fp32) or 8 (bf16) take the TMA-staged fast path, anything else a plain-load path.
+ * Any alignment and any dim are accepted; 16-byte aligned pointers with dim a multiple of 4
+ * (fp32) or 8 (bf16) take the TMA-staged fast path, anything else a plain-load path.
  *
  * Errors: argument checks are synchronous and return SSCAN_ERR_INVALID_ARG before anything is
  * launched; launch failures return SSCAN_ERR_CUDA. A device-side carry timeout (possible only
  * when the library splits one sequence across thread blocks) is recorded in a per-device status
  * word that sscan_get_device_error reports.
- * Workspace: when a sequence is split across thread blocks the library takes a small
- * stream-ordered scratch allocation (cudaMallocAsync on `stream`) and frees it stream-ordered.
+ * Workspace: on the fast path the library takes a stream-ordered scratch allocation
+ * (cudaMallocAsync on `stream`, freed stream-ordered) when it needs one: B and C widened to fp32
+ * rows of 16 states (bf16 inputs or N < 16: 128 bytes per batch row and step) and, when a long
+ * sequence is split across thread blocks, the chunk-carry flags and segment summaries.
  */
 sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias,
@@ -91,11 +93,12 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
  * allocation's possible synchronisation, or code whose memory budget is fixed up front.
  *
  * Arguments, layouts, results and errors are those of sscan_fwd; inputs and outputs are still
- * the caller's device buffers. The only difference is the chunk-carry scratch used when a long
- * sequence is split across thread blocks: instead of a stream-ordered allocation it lives in a
- * fixed 16 MiB array in device memory that every GPU which loads the library keeps until the
- * process exits. A call that would need more scratch than that (very long sequences with many
- * channels) returns SSCAN_ERR_SCRATCH_TOO_SMALL before launching anything; sscan_fwd serves it.
+ * the caller's device buffers. The only difference is the scratch sscan_fwd allocates per call
+ * (B and C widened to fp32, and the chunk-carry state of a sequence split across thread blocks):
+ * here it lives in a fixed 16 MiB array in device memory that every GPU which loads the library
+ * keeps until the process exits. A call that would need more than that (bf16 inputs or N < 16
+ * with more than about 120,000 batch rows x steps, or very long sequences split into many
+ * segments) returns SSCAN_ERR_SCRATCH_TOO_SMALL before launching anything; sscan_fwd serves it.
  *
  * - The first call on a device looks up that device's copy of the array (with the device
  *   current); make that first call before any stream capture.

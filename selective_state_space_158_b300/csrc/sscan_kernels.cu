@@ -87,8 +87,9 @@ __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_
 // Lane-owned kernel. Every lane owns one channel's K = 16 / G states (G = 1 or 2 lanes per
 // channel); a warp owns 32 / G whole channels, and does its prologue (softplus), recurrence,
 // readout, skip, gate and y store for them without leaving registers. The CTA shares only the
-// TMA-staged input tiles and the B / C rows, widened once per chunk to fp32 and read by every
-// lane as broadcast 16-byte loads. One CTA barrier per chunk orders the widening.
+// TMA-staged input tiles, including the fp32 B / C rows (16 states, zero-padded) that every lane
+// reads as broadcast 16-byte loads. Warps never wait for each other: each releases a stage
+// through an mbarrier when it has read it, and thread 0 refills a stage once every warp has.
 //
 // Long sequences are split into n_seg time segments run by different CTAs ("chunk carry"). The
 // scan operator (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) is associative ("架构变体：Mamba/SSM",
@@ -139,18 +140,17 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
 }
 
 struct LaneSmem {
-  size_t tile_io, bc_io, stage, off_stage, off_bc, off_y, y_warp, off_bar, total;
-  __host__ __device__ LaneSmem(int TC, int W, int CPW, int N, int es, int stages) {
+  size_t tile_io, bc_f32, stage, off_stage, off_y, y_warp, off_bar, total;
+  __host__ __device__ LaneSmem(int TC, int W, int CPW, int es, int stages) {
     const int CH = W * CPW;
     tile_io = align128(size_t(TC) * CH * es);
-    bc_io = align128(size_t(TC) * N * es);
-    stage = 3 * tile_io + 2 * bc_io;  // u, delta, z, B, C
+    bc_f32 = align128(size_t(TC) * kNP * sizeof(float));
+    stage = 3 * tile_io + 2 * bc_f32;  // u, delta, z (io); B, C (fp32, 16 states)
     off_stage = 0;
-    off_bc = size_t(stages) * stage;                       // [2][TC][2][16] fp32
-    y_warp = align128(size_t(TC) * CPW * es);               // one warp's y tile
-    off_y = off_bc + align128(size_t(2) * TC * 32 * sizeof(float));
-    off_bar = off_y + size_t(2) * W * y_warp;               // [2][W] y tiles
-    total = off_bar + 8 * 8 + 16;                           // mbarriers, ticket
+    y_warp = align128(size_t(TC) * CPW * es);            // one warp's y tile
+    off_y = size_t(stages) * stage;
+    off_bar = off_y + size_t(2) * W * y_warp;            // [2][W] y tiles
+    total = off_bar + 2 * 8 * 8 + 16;                    // full[8], empty[8], ticket
   }
 };
 
@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int W = nthr >> 5, CH = W * CPW;
   const int N = p.N, S = p.stages;
-  const LaneSmem lay(TC, W, CPW, N, int(sizeof(IO)), S);
-  float* bc0 = reinterpret_cast<float*>(smem + lay.off_bc);  // [2][TC][32]: B[0..15], C[0..15]
+  const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
-  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + lay.off_bar + 8 * 8);
+  uint64_t* empty = full + 8;
+  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + lay.off_bar + 2 * 8 * 8);
 
   // ---- which work this CTA does: channel group, batch row, time segment ----
   int cgi, b, seg;
@@ -203,10 +203,10 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   auto stage_ptr = [&](int s, int which) -> unsigned char* {  // 0 u, 1 delta, 2 z, 3 B, 4 C
     unsigned char* base = smem + lay.off_stage + size_t(s) * lay.stage;
     return which < 3 ? base + size_t(which) * lay.tile_io
-                     : base + 3 * lay.tile_io + size_t(which - 3) * lay.bc_io;
+                     : base + 3 * lay.tile_io + size_t(which - 3) * lay.bc_f32;
   };
   const uint32_t tile_bytes = uint32_t(TC) * CH * sizeof(IO);
-  const uint32_t bc_bytes = uint32_t(TC) * N * sizeof(IO);
+  const uint32_t bc_bytes = uint32_t(TC) * kNP * sizeof(float);
   const uint32_t stage_bytes = (p.has_z ? 3u : 2u) * tile_bytes + 2u * bc_bytes;
   // Load q (0 .. n_loads-1) brings chunk c_begin + q % nch into stage q % S.
   auto issue_load = [&](int q) {
@@ -226,7 +226,10 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
     tma_prefetch_desc(&tm_B);
     tma_prefetch_desc(&tm_C);
     tma_prefetch_desc(&tm_y);
-    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], W);
+    }
     mbar_init_fence();
   }
   __syncthreads();
@@ -298,31 +301,31 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       const int t0 = c * TC;
       const int t_valid = min(TC, p.L - t0);
       const bool landed = mbar_wait_bounded(&full[s], (q / S) & 1, kWaitTries);
-      const IO* B_s = reinterpret_cast<const IO*>(stage_ptr(s, 3));
-      const IO* C_s = reinterpret_cast<const IO*>(stage_ptr(s, 4));
-      float* bc = bc0 + (q & 1) * (TC * 32);
-      if (landed) {
-        for (int i = tid; i < TC * 32; i += nthr) {
-          const int t = i >> 5, k = i & 31, n = k & 15;
-          const IO* src = k < 16 ? B_s : C_s;
-          bc[i] = n < N ? to_f32(src[t * N + n]) : 0.f;
-        }
-      }
-      if (__syncthreads_or(!landed)) {  // CTA-uniform: every thread leaves together
+      if (__any_sync(0xffffffffu, !landed)) {  // warp-uniform: the whole warp leaves
         timed_out = true;
         break;
       }
-      // Every warp has finished load q-1, so its stage can take load q-1+S.
-      if (tid == 0 && q >= 1 && q - 1 + S < n_loads) issue_load(q - 1 + S);
+      // Thread 0 refills the stage of load q-1 once every warp has released it.
+      if (tid == 0 && q >= 1 && q - 1 + S < n_loads) {
+        const int sp = (q - 1) % S;
+        if (mbar_wait_bounded(&empty[sp], ((q - 1) / S) & 1, kWaitTries))
+          issue_load(q - 1 + S);
+        else
+          atomicOr(p.status, kErrTimeout);  // its waiters time out in turn
+      }
 
       const IO* u_s = reinterpret_cast<const IO*>(stage_ptr(s, 0)) + cl;
       const IO* dl_s = reinterpret_cast<const IO*>(stage_ptr(s, 1)) + cl;
       const IO* z_s = reinterpret_cast<const IO*>(stage_ptr(s, 2)) + cl;
+      const float* Bs = reinterpret_cast<const float*>(stage_ptr(s, 3));
+      const float* Cs = reinterpret_cast<const float*>(stage_ptr(s, 4));
 
       // Prologue, two steps at a time in f32x2: dt = softplus(delta + bias) and dt * u for
       // every step of the chunk (both lanes of a channel compute it when G == 2). Steps past
-      // the end of the sequence get dt = 0, an identity update.
-      float dt[TC], dtu[TC], uk[TC];
+      // the end of the sequence get dt = 0, an identity update. dt and dt*u are kept as
+      // duplicated pairs {v, v}, ready as packed-FMA operands.
+      float2 dtp[TC], dtup[TC];
+      float uk[TC];
 #pragma unroll
       for (int k = 0; k < TC / 2; ++k) {
         const int t = 2 * k;
@@ -332,10 +335,10 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
         if (p.softplus) d2 = softplus2(d2);
         d2 = f2(t < t_valid ? d2.x : 0.f, t + 1 < t_valid ? d2.y : 0.f);
         const float2 du = __fmul2_rn(d2, u2);
-        dt[t] = d2.x;
-        dt[t + 1] = d2.y;
-        dtu[t] = du.x;
-        dtu[t + 1] = du.y;
+        dtp[t] = f2(d2.x, d2.x);
+        dtp[t + 1] = f2(d2.y, d2.y);
+        dtup[t] = f2(du.x, du.x);
+        dtup[t + 1] = f2(du.y, du.y);
         uk[t] = u2.x;
         uk[t + 1] = u2.y;
       }
@@ -345,22 +348,23 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
         float csum = 0.f;
 #pragma unroll
         for (int t = 0; t < TC; ++t) {
-          const float4* Bq = reinterpret_cast<const float4*>(bc + t * 32 + n0);
-          const float2 dt2 = f2(dt[t], dt[t]), dtu2 = f2(dtu[t], dtu[t]);
-          csum += dt[t];
+          const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
+          csum += dtp[t].x;
 #pragma unroll
           for (int qq = 0; qq < K / 4; ++qq) {
             const float4 bq = Bq[qq];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int r = 2 * qq + j;
-              const float2 arg = __ffma2_rn(dt2, A2[r], f2(kEx2ArgShift, kEx2ArgShift));
+              const float2 arg = __ffma2_rn(dtp[t], A2[r], f2(kEx2ArgShift, kEx2ArgShift));
               const float2 dA = f2(ex2(arg.x), ex2(arg.y));
               const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
-              h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtu2, bb));
+              h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
         const float yk = csum - sd_c;  // Kahan step
         const float tk = sd + yk;
         sd_c = (tk - sd) - yk;
@@ -369,31 +373,29 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       }
 
       // Pass 2 (or the only pass): ZOH decay on the SFU, packed f32x2 FMAs for the state and
-      // the readout.
+      // the readout (four partial sums keep the dependency chains short).
       float ys[TC];
 #pragma unroll
       for (int t = 0; t < TC; ++t) {
-        const float4* Bq = reinterpret_cast<const float4*>(bc + t * 32 + n0);
-        const float4* Cq = reinterpret_cast<const float4*>(bc + t * 32 + 16 + n0);
-        const float2 dt2 = f2(dt[t], dt[t]), dtu2 = f2(dtu[t], dtu[t]);
-        float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+        const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
+        const float4* Cq = reinterpret_cast<const float4*>(Cs + t * kNP + n0);
+        float2 acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
         for (int qq = 0; qq < K / 4; ++qq) {
           const float4 bq = Bq[qq], cq = Cq[qq];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int r = 2 * qq + j;
-            const float2 arg = __ffma2_rn(dt2, A2[r], f2(kEx2ArgShift, kEx2ArgShift));
+            const float2 arg = __ffma2_rn(dtp[t], A2[r], f2(kEx2ArgShift, kEx2ArgShift));
             const float2 dA = f2(ex2(arg.x), ex2(arg.y));
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
-            h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtu2, bb));
-            if (j) acc1 = __ffma2_rn(cc, h[r], acc1);
-            else acc0 = __ffma2_rn(cc, h[r], acc0);
+            h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
+            acc[r & 3] = __ffma2_rn(cc, h[r], acc[r & 3]);
           }
         }
-        const float2 acc = __fadd2_rn(acc0, acc1);
-        ys[t] = acc.x + acc.y;
+        const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        ys[t] = a2.x + a2.y;
       }
 
       // Epilogue on this lane's own steps, two at a time: (readout + D u) * SiLU(z) into the
@@ -428,6 +430,7 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       fence_smem_to_async();
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&empty[s]);  // this warp is done with the stage (z read above)
         tma_store_3d(&tm_y, yw, ch0 + warp * CPW, t0, b);
         tma_store_commit();
       }
@@ -449,10 +452,7 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   }
 
   if (timed_out) {
-    if (tid == 0) {
-      atomicOr(p.status, kErrTimeout);
-      for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 1024);
-    }
+    if (lane == 0) atomicOr(p.status, kErrTimeout);
   } else if (p.h_last && live && seg == p.n_seg - 1) {
     float* dst = p.h_last + (size_t(b) * p.dim + cg) * N;
 #pragma unroll
@@ -463,6 +463,36 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
     }
   }
   if (lane == 0) tma_store_wait_all();
+  // Loads still in flight (issued for chunks that were never consumed after a timeout) get a
+  // bounded chance to land before the CTA's shared memory goes away.
+  __syncthreads();
+  if (tid == 0 && timed_out)
+    for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 1024);
+}
+
+// B and C widened once per call to fp32 rows of 16 states (zero-padded past N), the layout the
+// scan kernel stages with TMA and reads as 16-byte vectors. One thread per (batch, step) row.
+template <typename IO>
+__global__ void __launch_bounds__(256) sscan_bc_widen_kernel(const IO* __restrict__ B,
+                                                             const IO* __restrict__ C, int N,
+                                                             int64_t rows, float* __restrict__ B16,
+                                                             float* __restrict__ C16) {
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r < rows;
+       r += int64_t(gridDim.x) * blockDim.x) {
+    float vb[kNP], vc[kNP];
+#pragma unroll
+    for (int n = 0; n < kNP; ++n) {
+      vb[n] = n < N ? to_f32(B[r * N + n]) : 0.f;
+      vc[n] = n < N ? to_f32(C[r * N + n]) : 0.f;
+    }
+    float4* ob = reinterpret_cast<float4*>(B16 + r * kNP);
+    float4* oc = reinterpret_cast<float4*>(C16 + r * kNP);
+#pragma unroll
+    for (int k = 0; k < kNP / 4; ++k) {
+      ob[k] = make_float4(vb[4 * k], vb[4 * k + 1], vb[4 * k + 2], vb[4 * k + 3]);
+      oc[k] = make_float4(vc[4 * k], vc[4 * k + 1], vc[4 * k + 2], vc[4 * k + 3]);
+    }
+  }
 }
 
 // ================================================================================================
@@ -549,33 +579,26 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   const int es = a.io == Io::F32 ? 4 : 2;
   if (stages < 2 || stages > 8) stages = 3;
   while (stages > 2 &&
-         LaneSmem(kLaneTC, W, CPW, int(a.N), es, stages).total + 128 > size_t(227) * 1024)
+         LaneSmem(kLaneTC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
     --stages;
   p.stages = stages;
-  const LaneSmem lay(kLaneTC, W, CPW, int(a.N), es, stages);
+  const LaneSmem lay(kLaneTC, W, CPW, es, stages);
   const size_t smem_bytes = lay.total + 128;
   if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
-  CUtensorMap mu, md, mz, mB, mC, my;
-  const uint64_t dim = a.dim, L = a.L, bt = a.batch, N = a.N;
-  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&md, a.delta, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&mB, a.B, a.io, N, L, bt, uint32_t(N), kLaneTC) &&
-            make_map(&mC, a.C, a.io, N, L, bt, uint32_t(N), kLaneTC) &&
-            make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
-  if (!ok) return cudaErrorInvalidValue;
-  auto kern = sscan_lane_kernel<IO, G, kLaneTC>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
-  if (e != cudaSuccess) return e;
+
+  // Scratch: B and C widened to fp32 rows of 16 states (unless they already are), then the
+  // chunk-carry ticket, flags and aggregates. Stream-ordered allocation, or the caller's buffer.
+  const bool widen = a.io != Io::F32 || a.N != kNP;
+  const size_t rows = size_t(a.batch) * size_t(a.L);
+  const size_t bc_bytes = widen ? align128(rows * kNP * sizeof(float)) : 0;
+  const size_t units = n_seg > 1 ? size_t(n_seg) * warps_per_seg : 0;
+  const size_t flag_bytes = n_seg > 1 ? align128(sizeof(unsigned) * (1 + units)) : 0;
+  const size_t carry_bytes = n_seg > 1 ? flag_bytes + units * 32 * (K + 1) * sizeof(float) : 0;
+  const size_t bytes = 2 * bc_bytes + carry_bytes;
   void* ws = nullptr;
   const bool own_ws = a.scratch == nullptr;
-  if (n_seg > 1) {
-    // Workspace: ticket, flags, aggregates. Stream-ordered allocation, or the caller's fixed
-    // scratch.
-    const size_t units = size_t(n_seg) * warps_per_seg;
-    const size_t flag_bytes = align128(sizeof(unsigned) * (1 + units));
-    const size_t bytes = flag_bytes + units * 32 * (K + 1) * sizeof(float);
+  cudaError_t e = cudaSuccess;
+  if (bytes > 0) {
     if (own_ws) {
       e = cudaMallocAsync(&ws, bytes, a.stream);
       if (e != cudaSuccess) return e;
@@ -586,18 +609,60 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
       }
       ws = a.scratch;
     }
-    e = cudaMemsetAsync(ws, 0, flag_bytes, a.stream);
-    if (e != cudaSuccess) {
-      if (own_ws) cudaFreeAsync(ws, a.stream);
-      return e;
+  }
+  auto release = [&](cudaError_t err) {
+    if (ws && own_ws) {
+      cudaError_t e2 = cudaFreeAsync(ws, a.stream);
+      if (err == cudaSuccess) err = e2;
     }
-    p.ticket = static_cast<unsigned*>(ws);
+    return err;
+  };
+  char* wsb = static_cast<char*>(ws);
+  const void* B16 = a.B;
+  const void* C16 = a.C;
+  if (widen) {
+    float* b16 = reinterpret_cast<float*>(wsb);
+    float* c16 = reinterpret_cast<float*>(wsb + bc_bytes);
+    const int wthreads = 256;
+    const unsigned wblocks =
+        unsigned(std::min<size_t>((rows + wthreads - 1) / wthreads, size_t(148) * 64));
+    if (a.io == Io::F32)
+      sscan_bc_widen_kernel<float><<<wblocks, wthreads, 0, a.stream>>>(
+          static_cast<const float*>(a.B), static_cast<const float*>(a.C), int(a.N), int64_t(rows),
+          b16, c16);
+    else
+      sscan_bc_widen_kernel<__nv_bfloat16><<<wblocks, wthreads, 0, a.stream>>>(
+          static_cast<const __nv_bfloat16*>(a.B), static_cast<const __nv_bfloat16*>(a.C),
+          int(a.N), int64_t(rows), b16, c16);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return release(e);
+    B16 = b16;
+    C16 = c16;
+  }
+  if (n_seg > 1) {
+    char* carry = wsb + 2 * bc_bytes;
+    e = cudaMemsetAsync(carry, 0, flag_bytes, a.stream);
+    if (e != cudaSuccess) return release(e);
+    p.ticket = reinterpret_cast<unsigned*>(carry);
     p.flags = p.ticket + 1;
-    p.agg = reinterpret_cast<float*>(static_cast<char*>(ws) + flag_bytes);
+    p.agg = reinterpret_cast<float*>(carry + flag_bytes);
   } else {
     p.ticket = p.flags = nullptr;
     p.agg = nullptr;
   }
+
+  CUtensorMap mu, md, mz, mB, mC, my;
+  const uint64_t dim = a.dim, L = a.L, bt = a.batch;
+  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&md, a.delta, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, kLaneTC) &&
+            make_map(&mB, B16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
+            make_map(&mC, C16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
+            make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
+  if (!ok) return release(cudaErrorInvalidValue);
+  auto kern = sscan_lane_kernel<IO, G, kLaneTC>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
+  if (e != cudaSuccess) return release(e);
   if (n_seg > 1) {
     kern<<<unsigned(n_seg * warps_per_seg / W), threads, smem_bytes, a.stream>>>(mu, md, mz, mB,
                                                                                  mC, my, p);
@@ -605,12 +670,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
     dim3 grid(unsigned(p.n_cg), unsigned(bt), 1);
     kern<<<grid, threads, smem_bytes, a.stream>>>(mu, md, mz, mB, mC, my, p);
   }
-  e = cudaGetLastError();
-  if (ws && own_ws) {
-    cudaError_t e2 = cudaFreeAsync(ws, a.stream);
-    if (e == cudaSuccess) e = e2;
-  }
-  return e;
+  return release(cudaGetLastError());
 }
 
 }  // namespace
@@ -651,7 +711,7 @@ bool tma_path_ok(const FwdArgs& a) {
   if (!aligned16(a.u) || !aligned16(a.delta) || !aligned16(a.B) || !aligned16(a.C) ||
       !aligned16(a.y) || (a.z && !aligned16(a.z)))
     return false;
-  if ((a.dim * es) % 16 != 0 || (a.N * es) % 16 != 0) return false;
+  if ((a.dim * es) % 16 != 0) return false;  // B / C are re-laid out when not fp32 x 16
   if (a.L > INT32_MAX - 64 || a.dim > INT32_MAX || a.batch > 65535) return false;
   return get_encode() != nullptr;
 }
