@@ -30,7 +30,7 @@
 namespace sscan {
 
 constexpr int kNP = 16;          // states held per channel (N <= 16 is zero-padded to 16)
-constexpr uint32_t kWaitTries = 1u << 22;  // bound on one mbarrier wait (seconds, not forever)
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on one mbarrier wait: one second
 constexpr unsigned kErrTimeout = 1u << 4;  // status bit: a bounded wait ran out
 
 // ================================================================================================
@@ -88,8 +88,8 @@ __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_
 // channel); a warp owns 32 / G whole channels, and does its prologue (softplus), recurrence,
 // readout, skip, gate and y store for them without leaving registers. The CTA shares only the
 // TMA-staged input tiles, including the fp32 B / C rows (16 states, zero-padded) that every lane
-// reads as broadcast 16-byte loads. Warps never wait for each other: each releases a stage
-// through an mbarrier when it has read it, and thread 0 refills a stage once every warp has.
+// reads as broadcast 16-byte loads. Warps never wait for each other: each counts itself out of a
+// stage when it has read it, and the last warp to do so issues the stage's refill.
 //
 // Long sequences are split into n_seg time segments run by different CTAs ("chunk carry"). The
 // scan operator (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) is associative ("架构变体：Mamba/SSM",
@@ -150,12 +150,60 @@ struct LaneSmem {
     y_warp = align128(size_t(TC) * CPW * es);            // one warp's y tile
     off_y = size_t(stages) * stage;
     off_bar = off_y + size_t(2) * W * y_warp;            // [2][W] y tiles
-    total = off_bar + 2 * 8 * 8 + 16;                    // full[8], empty[8], ticket
+    total = off_bar + 8 * 8 + 8 * 4 + 16;                // full[8], done[8], ticket
   }
 };
 
+// Cross-lane transpose-reduce of per-step partial readouts: on entry every lane of a channel's
+// G-lane group holds its partial sum for all TC steps; on exit lane g holds the full readout of
+// the steps t = g + G k (k = 0 .. TC/G - 1) in out[k]. One shuffle per value and round.
+template <int G, int TC>
+__device__ __forceinline__ void reduce_transpose(const float (&ys)[TC], float (&out)[TC / G],
+                                                 int g) {
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int k = 0; k < TC; ++k) out[k] = ys[k];
+  } else if constexpr (G == 2) {
+#pragma unroll
+    for (int k = 0; k < TC / 2; ++k) {
+      const float lo = ys[2 * k], hi = ys[2 * k + 1];
+      out[k] = (g ? hi : lo) + __shfl_xor_sync(0xffffffffu, g ? lo : hi, 1);
+    }
+  } else {
+    static_assert(G == 4, "G must be 1, 2 or 4");
+    // Round 1 (partner lane ^ 2) keeps the steps whose bit 1 matches g's; round 2 (lane ^ 1)
+    // the ones whose bit 0 does.
+    const bool hi2 = (g & 2) != 0, hi1 = (g & 1) != 0;
+    float r1[TC / 2];
+#pragma unroll
+    for (int m = 0; m < TC / 2; ++m) {
+      const int t0 = (m >> 1) * 4 + (m & 1), t1 = t0 + 2;
+      r1[m] = (hi2 ? ys[t1] : ys[t0]) + __shfl_xor_sync(0xffffffffu, hi2 ? ys[t0] : ys[t1], 2);
+    }
+#pragma unroll
+    for (int k = 0; k < TC / 4; ++k) {
+      const float lo = r1[2 * k], hi = r1[2 * k + 1];
+      out[k] = (hi1 ? hi : lo) + __shfl_xor_sync(0xffffffffu, hi1 ? lo : hi, 1);
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_shared(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_addr(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Register budget: up to 255 registers with one or two lanes per channel; with four there are
+// more warps to keep resident, so at most 128.
+template <int G>
+__host__ __device__ constexpr int lane_min_blocks() { return G == 4 ? 2 : 1; }
+
 template <typename IO, int G, int TC>
-__global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
+__global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
     const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
@@ -163,7 +211,7 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   constexpr int K = kNP / G;     // states per lane
   constexpr int KP = K / 2;      // float2 state registers per lane (states n, n+1 packed)
   constexpr int CPW = 32 / G;    // channels per warp
-  static_assert(G == 1 || G == 2, "G must be 1 or 2");
+  static_assert(G == 1 || G == 2 || G == 4, "G must be 1, 2 or 4");
   static_assert(TC % 2 == 0, "chunk must be even");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
@@ -173,8 +221,8 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   const int N = p.N, S = p.stages;
   const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
-  uint64_t* empty = full + 8;
-  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + lay.off_bar + 2 * 8 * 8);
+  unsigned* done = reinterpret_cast<unsigned*>(smem + lay.off_bar + 8 * 8);
+  unsigned* s_ticket = done + 8;
 
   // ---- which work this CTA does: channel group, batch row, time segment ----
   int cgi, b, seg;
@@ -219,6 +267,19 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
     tma_load_3d(stage_ptr(s, 3), &tm_B, 0, t0, b, &full[s]);
     tma_load_3d(stage_ptr(s, 4), &tm_C, 0, t0, b, &full[s]);
   };
+  // A warp done with stage s (load q) counts itself out; the last of the W warps refills it
+  // with load q + S. The acquire-release count orders every warp's reads of the stage before
+  // the refill's TMA writes.
+  auto release_stage = [&](int s, int q) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0 && atom_add_acq_rel_shared(&done[s], 1u) == unsigned(W - 1)) {
+      done[s] = 0;
+      if (q + S < n_loads) {
+        fence_smem_to_async();
+        issue_load(q + S);
+      }
+    }
+  };
   if (tid == 0) {
     tma_prefetch_desc(&tm_u);
     tma_prefetch_desc(&tm_dl);
@@ -228,7 +289,7 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
     tma_prefetch_desc(&tm_y);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], W);
+      done[s] = 0;
     }
     mbar_init_fence();
   }
@@ -300,18 +361,10 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       const int s = q % S;
       const int t0 = c * TC;
       const int t_valid = min(TC, p.L - t0);
-      const bool landed = mbar_wait_bounded(&full[s], (q / S) & 1, kWaitTries);
+      const bool landed = mbar_wait_bounded(&full[s], (q / S) & 1, kWaitNs);
       if (__any_sync(0xffffffffu, !landed)) {  // warp-uniform: the whole warp leaves
         timed_out = true;
         break;
-      }
-      // Thread 0 refills the stage of load q-1 once every warp has released it.
-      if (tid == 0 && q >= 1 && q - 1 + S < n_loads) {
-        const int sp = (q - 1) % S;
-        if (mbar_wait_bounded(&empty[sp], ((q - 1) / S) & 1, kWaitTries))
-          issue_load(q - 1 + S);
-        else
-          atomicOr(p.status, kErrTimeout);  // its waiters time out in turn
       }
 
       const IO* u_s = reinterpret_cast<const IO*>(stage_ptr(s, 0)) + cl;
@@ -320,27 +373,53 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       const float* Bs = reinterpret_cast<const float*>(stage_ptr(s, 3));
       const float* Cs = reinterpret_cast<const float*>(stage_ptr(s, 4));
 
-      // Prologue, two steps at a time in f32x2: dt = softplus(delta + bias) and dt * u for
-      // every step of the chunk (both lanes of a channel compute it when G == 2). Steps past
-      // the end of the sequence get dt = 0, an identity update. dt and dt*u are kept as
-      // duplicated pairs {v, v}, ready as packed-FMA operands.
-      float2 dtp[TC], dtup[TC];
-      float uk[TC];
+      // Prologue: dt = softplus(delta + bias) and dt * u, two steps at a time in f32x2, kept as
+      // duplicated pairs {v, v} for all TC steps, ready as packed-FMA operands. With one or two
+      // lanes per channel every lane computes all TC steps (recomputing is cheaper than trading
+      // them); with four, lane g computes only its own steps t = g + 4 k and the four lanes
+      // trade them with shuffles. Steps past the end of the sequence get dt = 0, an identity
+      // update. uo keeps u of this lane's own output steps for the skip term.
+      constexpr int OWN = TC / G;
+      constexpr bool kShare = G == 4;
+      constexpr int NP = kShare ? OWN : TC;  // steps this lane computes
+      float own_dt[NP], own_du[NP], own_u[NP], uo[OWN];
 #pragma unroll
-      for (int k = 0; k < TC / 2; ++k) {
-        const int t = 2 * k;
-        const float2 u2 = f2(to_f32(u_s[t * CH]), to_f32(u_s[(t + 1) * CH]));
-        float2 d2 = __fadd2_rn(f2(to_f32(dl_s[t * CH]), to_f32(dl_s[(t + 1) * CH])),
+      for (int k = 0; k < NP; k += 2) {
+        const int ta = kShare ? g + G * k : k, tb = kShare ? ta + G : k + 1;
+        const float2 u2 = f2(to_f32(u_s[ta * CH]), to_f32(u_s[tb * CH]));
+        float2 d2 = __fadd2_rn(f2(to_f32(dl_s[ta * CH]), to_f32(dl_s[tb * CH])),
                                f2(bias_c, bias_c));
         if (p.softplus) d2 = softplus2(d2);
-        d2 = f2(t < t_valid ? d2.x : 0.f, t + 1 < t_valid ? d2.y : 0.f);
+        d2 = f2(ta < t_valid ? d2.x : 0.f, tb < t_valid ? d2.y : 0.f);
         const float2 du = __fmul2_rn(d2, u2);
-        dtp[t] = f2(d2.x, d2.x);
-        dtp[t + 1] = f2(d2.y, d2.y);
-        dtup[t] = f2(du.x, du.x);
-        dtup[t + 1] = f2(du.y, du.y);
-        uk[t] = u2.x;
-        uk[t + 1] = u2.y;
+        own_dt[k] = d2.x;
+        own_dt[k + 1] = d2.y;
+        own_du[k] = du.x;
+        own_du[k + 1] = du.y;
+        own_u[k] = u2.x;
+        own_u[k + 1] = u2.y;
+      }
+      float2 dtp[TC], dtup[TC];
+#pragma unroll
+      for (int t = 0; t < TC; ++t) {
+        float dt, du;
+        if constexpr (kShare) {  // step t belongs to lane t % G of this channel's group
+          const int src = (lane & ~(G - 1)) | (t % G);
+          dt = __shfl_sync(0xffffffffu, own_dt[t / G], src);
+          du = __shfl_sync(0xffffffffu, own_du[t / G], src);
+        } else {
+          dt = own_dt[t];
+          du = own_du[t];
+        }
+        dtp[t] = f2(dt, dt);
+        dtup[t] = f2(du, du);
+      }
+#pragma unroll
+      for (int k = 0; k < OWN; ++k) {
+        if constexpr (kShare || G == 1)
+          uo[k] = own_u[k];
+        else
+          uo[k] = g ? own_u[G * k + 1] : own_u[G * k];
       }
 
       if (!readout) {
@@ -363,8 +442,7 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+        release_stage(s, q);
         const float yk = csum - sd_c;  // Kahan step
         const float tk = sd + yk;
         sd_c = (tk - sd) - yk;
@@ -399,28 +477,16 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
       }
 
       // Epilogue on this lane's own steps, two at a time: (readout + D u) * SiLU(z) into the
-      // warp's y tile. With G == 2 the partner lanes first trade partial readouts so that lane
-      // g holds the full readout of steps t + g.
+      // warp's y tile. With G > 1 the lanes of a channel first combine their partial readouts
+      // so that lane g holds the full readout of its steps t = g + G k.
       if (lane == 0 && ystores >= 2) tma_store_wait_read<1>();  // tile of two stores ago read
       __syncwarp();
       IO* yw = ywarp0 + size_t(ystores & 1) * (size_t(W) * lay.y_warp / sizeof(IO));
-      constexpr int OWN = TC / G;
-      float yo[OWN], uo[OWN];
-#pragma unroll
-      for (int k = 0; k < OWN; ++k) {
-        if constexpr (G == 1) {
-          yo[k] = ys[k];
-          uo[k] = uk[k];
-        } else {
-          const int t = 2 * k;
-          const float send = g ? ys[t] : ys[t + 1], keep = g ? ys[t + 1] : ys[t];
-          yo[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-          uo[k] = g ? uk[t + 1] : uk[t];
-        }
-      }
+      float yo[OWN];
+      reduce_transpose<G, TC>(ys, yo, g);
 #pragma unroll
       for (int k = 0; k < OWN; k += 2) {
-        const int ta = G * k + g, tb = G * (k + 1) + g;  // this lane's steps
+        const int ta = g + G * k, tb = ta + G;  // this lane's steps
         float2 y2 = __ffma2_rn(f2(D_c, D_c), f2(uo[k], uo[k + 1]), f2(yo[k], yo[k + 1]));
         if (p.has_z)
           y2 = __fmul2_rn(y2, silu2(f2(to_f32(z_s[ta * CH]), to_f32(z_s[tb * CH]))));
@@ -428,9 +494,8 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
         store_io(yw + tb * CPW + lane / G, y2.y);
       }
       fence_smem_to_async();
-      __syncwarp();
+      release_stage(s, q);  // z was the stage's last use
       if (lane == 0) {
-        mbar_arrive(&empty[s]);  // this warp is done with the stage (z read above)
         tma_store_3d(&tm_y, yw, ch0 + warp * CPW, t0, b);
         tma_store_commit();
       }
@@ -465,9 +530,9 @@ __global__ void __launch_bounds__(256, 1) sscan_lane_kernel(
   if (lane == 0) tma_store_wait_all();
   // Loads still in flight (issued for chunks that were never consumed after a timeout) get a
   // bounded chance to land before the CTA's shared memory goes away.
-  __syncthreads();
-  if (tid == 0 && timed_out)
-    for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 1024);
+  const int any_timeout = __syncthreads_or(timed_out);
+  if (tid == 0 && any_timeout)
+    for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 100000);
 }
 
 // B and C widened once per call to fp32 rows of 16 states (zero-padded past N), the layout the
@@ -543,83 +608,56 @@ int env_int_or(const char* name, int dflt) {
 }
 
 constexpr int kLaneTC = 16;
+constexpr int64_t kSplitBelowWarps = 300;  // fewer warps than this: split the sequence
 
-template <typename IO, int G>
-cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
-  constexpr int CPW = 32 / G;
-  constexpr int K = kNP / G;
-  const int W = threads / 32;
-  const int CH = W * CPW;
-  LaneParams p;
-  p.A = a.A;
-  p.D = a.D;
-  p.bias = a.bias;
-  p.h_last = a.h_last;
-  p.status = a.status;
-  p.L = int(a.L);
-  p.dim = int(a.dim);
-  p.N = int(a.N);
-  p.batch = int(a.batch);
-  p.softplus = a.softplus;
-  p.has_z = a.z != nullptr;
-  p.n_chunks = int((a.L + kLaneTC - 1) / kLaneTC);
-  p.n_cg = int((a.dim + CH - 1) / CH);
-  // Chunk carry: split the sequence when too few warps would run otherwise (about 2 per SM).
-  const int64_t warps_per_seg = a.batch * p.n_cg * W;
-  int n_seg = segments;
-  if (n_seg <= 0) {
-    n_seg = 1;
-    if (warps_per_seg < 300) n_seg = int((148 * 16 + warps_per_seg - 1) / warps_per_seg);
+// Per-call scratch: B and C widened to fp32 rows of 16 states (unless they already are), then
+// the chunk-carry ticket, flags and aggregates (carry_units warp units of 32 lanes x (K + 1)
+// floats). Stream-ordered allocation, or the caller's buffer.
+struct Workspace {
+  const void* B16 = nullptr;
+  const void* C16 = nullptr;
+  unsigned* ticket = nullptr;
+  unsigned* flags = nullptr;
+  float* agg = nullptr;
+  void* mem = nullptr;
+  bool own = false;
+  cudaStream_t stream = nullptr;
+  cudaError_t release(cudaError_t err) {
+    if (mem && own) {
+      cudaError_t e2 = cudaFreeAsync(mem, stream);
+      if (err == cudaSuccess) err = e2;
+    }
+    mem = nullptr;
+    return err;
   }
-  n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
-  p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
-  n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;  // no empty segments
-  p.n_seg = n_seg;
-  p.skip_publish = env_int_or("SSCAN_TEST_SKIP_PUBLISH", -1);
-  const int es = a.io == Io::F32 ? 4 : 2;
-  if (stages < 2 || stages > 8) stages = 3;
-  while (stages > 2 &&
-         LaneSmem(kLaneTC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
-    --stages;
-  p.stages = stages;
-  const LaneSmem lay(kLaneTC, W, CPW, es, stages);
-  const size_t smem_bytes = lay.total + 128;
-  if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
+};
 
-  // Scratch: B and C widened to fp32 rows of 16 states (unless they already are), then the
-  // chunk-carry ticket, flags and aggregates. Stream-ordered allocation, or the caller's buffer.
+cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Workspace* w) {
+  w->stream = a.stream;
   const bool widen = a.io != Io::F32 || a.N != kNP;
   const size_t rows = size_t(a.batch) * size_t(a.L);
   const size_t bc_bytes = widen ? align128(rows * kNP * sizeof(float)) : 0;
-  const size_t units = n_seg > 1 ? size_t(n_seg) * warps_per_seg : 0;
-  const size_t flag_bytes = n_seg > 1 ? align128(sizeof(unsigned) * (1 + units)) : 0;
-  const size_t carry_bytes = n_seg > 1 ? flag_bytes + units * 32 * (K + 1) * sizeof(float) : 0;
+  const size_t flag_bytes = carry_units ? align128(sizeof(unsigned) * (1 + carry_units)) : 0;
+  const size_t carry_bytes =
+      carry_units ? flag_bytes + carry_units * 32 * (K + 1) * sizeof(float) : 0;
   const size_t bytes = 2 * bc_bytes + carry_bytes;
-  void* ws = nullptr;
-  const bool own_ws = a.scratch == nullptr;
+  w->own = a.scratch == nullptr;
   cudaError_t e = cudaSuccess;
   if (bytes > 0) {
-    if (own_ws) {
-      e = cudaMallocAsync(&ws, bytes, a.stream);
+    if (w->own) {
+      e = cudaMallocAsync(&w->mem, bytes, a.stream);
       if (e != cudaSuccess) return e;
     } else {
       if (bytes > a.scratch_bytes) {
         if (a.scratch_short) *a.scratch_short = true;
         return cudaErrorInvalidValue;
       }
-      ws = a.scratch;
+      w->mem = a.scratch;
     }
   }
-  auto release = [&](cudaError_t err) {
-    if (ws && own_ws) {
-      cudaError_t e2 = cudaFreeAsync(ws, a.stream);
-      if (err == cudaSuccess) err = e2;
-    }
-    return err;
-  };
-  char* wsb = static_cast<char*>(ws);
-  const void* B16 = a.B;
-  const void* C16 = a.C;
+  char* wsb = static_cast<char*>(w->mem);
+  w->B16 = a.B;
+  w->C16 = a.C;
   if (widen) {
     float* b16 = reinterpret_cast<float*>(wsb);
     float* c16 = reinterpret_cast<float*>(wsb + bc_bytes);
@@ -635,66 +673,131 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
           static_cast<const __nv_bfloat16*>(a.B), static_cast<const __nv_bfloat16*>(a.C),
           int(a.N), int64_t(rows), b16, c16);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return release(e);
-    B16 = b16;
-    C16 = c16;
+    if (e != cudaSuccess) return w->release(e);
+    w->B16 = b16;
+    w->C16 = c16;
   }
-  if (n_seg > 1) {
+  if (carry_units) {
     char* carry = wsb + 2 * bc_bytes;
     e = cudaMemsetAsync(carry, 0, flag_bytes, a.stream);
-    if (e != cudaSuccess) return release(e);
-    p.ticket = reinterpret_cast<unsigned*>(carry);
-    p.flags = p.ticket + 1;
-    p.agg = reinterpret_cast<float*>(carry + flag_bytes);
-  } else {
-    p.ticket = p.flags = nullptr;
-    p.agg = nullptr;
+    if (e != cudaSuccess) return w->release(e);
+    w->ticket = reinterpret_cast<unsigned*>(carry);
+    w->flags = w->ticket + 1;
+    w->agg = reinterpret_cast<float*>(carry + flag_bytes);
   }
+  return cudaSuccess;
+}
+
+// Common launch parameters; segments: time segments requested (0: automatic, for `units_per_seg`
+// warp units of state).
+LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64_t units_per_seg) {
+  LaneParams p;
+  p.A = a.A;
+  p.D = a.D;
+  p.bias = a.bias;
+  p.h_last = a.h_last;
+  p.status = a.status;
+  p.L = int(a.L);
+  p.dim = int(a.dim);
+  p.N = int(a.N);
+  p.batch = int(a.batch);
+  p.softplus = a.softplus;
+  p.has_z = a.z != nullptr;
+  p.n_chunks = int((a.L + kLaneTC - 1) / kLaneTC);
+  p.n_cg = int((a.dim + CH - 1) / CH);
+  p.stages = stages;
+  // Chunk carry: split the sequence when too few warps would run otherwise (about 2 per SM),
+  // into enough segments for about 40 warps per SM (measured best on B300 for a long sequence).
+  int n_seg = segments;
+  if (n_seg <= 0) {
+    n_seg = 1;
+    if (units_per_seg < kSplitBelowWarps)
+      n_seg = int((148 * 40 + units_per_seg - 1) / units_per_seg);
+  }
+  n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
+  p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
+  p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;  // no empty segments
+  p.skip_publish = env_int_or("SSCAN_TEST_SKIP_PUBLISH", -1);
+  p.ticket = p.flags = nullptr;
+  p.agg = nullptr;
+  return p;
+}
+
+template <typename IO, int G>
+cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
+  constexpr int CPW = 32 / G;
+  constexpr int K = kNP / G;
+  const int W = threads / 32;
+  const int CH = W * CPW;
+  const int es = a.io == Io::F32 ? 4 : 2;
+  if (stages < 2 || stages > 8) stages = 3;
+  while (stages > 2 &&
+         LaneSmem(kLaneTC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
+    --stages;
+  const LaneSmem lay(kLaneTC, W, CPW, es, stages);
+  const size_t smem_bytes = lay.total + 128;
+  if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
+  const int64_t n_cg = (a.dim + CH - 1) / CH;
+  const int64_t warps_per_seg = a.batch * n_cg * W;
+  LaneParams p = base_params(a, CH, stages, segments, warps_per_seg);
+
+  Workspace w;
+  cudaError_t e = prepare_workspace(a, p.n_seg > 1 ? size_t(p.n_seg) * warps_per_seg : 0, K, &w);
+  if (e != cudaSuccess) return e;
+  p.ticket = w.ticket;
+  p.flags = w.flags;
+  p.agg = w.agg;
 
   CUtensorMap mu, md, mz, mB, mC, my;
   const uint64_t dim = a.dim, L = a.L, bt = a.batch;
   bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, kLaneTC) &&
             make_map(&md, a.delta, a.io, dim, L, bt, CH, kLaneTC) &&
             make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&mB, B16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
-            make_map(&mC, C16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
+            make_map(&mB, w.B16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
+            make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
             make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
-  if (!ok) return release(cudaErrorInvalidValue);
+  if (!ok) return w.release(cudaErrorInvalidValue);
   auto kern = sscan_lane_kernel<IO, G, kLaneTC>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
-  if (e != cudaSuccess) return release(e);
-  if (n_seg > 1) {
-    kern<<<unsigned(n_seg * warps_per_seg / W), threads, smem_bytes, a.stream>>>(mu, md, mz, mB,
-                                                                                 mC, my, p);
+  if (e != cudaSuccess) return w.release(e);
+  if (p.n_seg > 1) {
+    kern<<<unsigned(p.n_seg * warps_per_seg / W), threads, smem_bytes, a.stream>>>(mu, md, mz, mB,
+                                                                                   mC, my, p);
   } else {
     dim3 grid(unsigned(p.n_cg), unsigned(bt), 1);
     kern<<<grid, threads, smem_bytes, a.stream>>>(mu, md, mz, mB, mC, my, p);
   }
-  return release(cudaGetLastError());
+  return w.release(cudaGetLastError());
 }
 
 }  // namespace
 
 cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
-  // One lane per channel (16 states) when there are enough channels to fill the SMs, else two
-  // lanes per channel; when even that leaves fewer than about two warps per SM the sequence is
-  // split into time segments (chunk carry) and one lane per channel is used again.
-  const int threads = tune.threads ? tune.threads : 128;
-  if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
+  // Layout from the number of channels (batch x dim), measured on B300: one lane per channel
+  // (16 states per lane, 256-thread CTAs) from about 24k channels up; two lanes (128 threads)
+  // from about 16k; four lanes (64 threads) below that. When the sequence will be split into
+  // time segments anyway (too few warps even with four lanes), one lane per channel again.
   const int64_t chans = a.batch * a.dim;
   int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
   if (G == 0) {
-    G = chans >= 148 * 128 ? 1 : 2;
-    if (chans * 2 / 32 < 300) G = 1;  // time segments will supply the parallelism
+    G = chans >= 24576 ? 1 : (chans >= 16384 ? 2 : 4);
+    if (chans * 4 / 32 < kSplitBelowWarps) G = 1;
   }
+  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
+  if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
-  if (G != 1 && G != 2) return cudaErrorInvalidValue;
+  if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
-  if (a.io == Io::F32)
-    return G == 1 ? launch_lane_typed<float, 1>(a, threads, tune.stages, tune.segments)
-                  : launch_lane_typed<float, 2>(a, threads, tune.stages, tune.segments);
-  return G == 1 ? launch_lane_typed<__nv_bfloat16, 1>(a, threads, tune.stages, tune.segments)
-                : launch_lane_typed<__nv_bfloat16, 2>(a, threads, tune.stages, tune.segments);
+  const int st = tune.stages, sg = tune.segments;
+  if (a.io == Io::F32) {
+    if (G == 1) return launch_lane_typed<float, 1>(a, threads, st, sg);
+    if (G == 2) return launch_lane_typed<float, 2>(a, threads, st, sg);
+    return launch_lane_typed<float, 4>(a, threads, st, sg);
+  }
+  using bf = __nv_bfloat16;
+  if (G == 1) return launch_lane_typed<bf, 1>(a, threads, st, sg);
+  if (G == 2) return launch_lane_typed<bf, 2>(a, threads, st, sg);
+  return launch_lane_typed<bf, 4>(a, threads, st, sg);
 }
 
 TmaTuning tuning_from_env() {
@@ -703,6 +806,7 @@ TmaTuning tuning_from_env() {
   t.segments = env_int("SSCAN_SEGMENTS");
   t.threads = env_int("SSCAN_THREADS");
   t.stages = env_int("SSCAN_STAGES");
+
   return t;
 }
 

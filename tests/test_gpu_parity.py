@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 ENV_KEYS = ("SSCAN_K", "SSCAN_THREADS", "SSCAN_STAGES", "SSCAN_PATH", "SSCAN_SEGMENTS",
             "SSCAN_TEST_SKIP_PUBLISH")
-STATES_PER_LANE = [16, 8]  # one or two lanes per channel
+STATES_PER_LANE = [16, 8, 4]  # one, two or four lanes per channel
 
 
 @pytest.fixture(autouse=True)
