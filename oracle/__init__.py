@@ -59,6 +59,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sscan_oracle_channel.argtypes = [vp, vp, vp, i64, fp, vp, vp, fp, fp, ci,
                                          i64, i64, ci, dp, i64, dp, dp]
     lib.sscan_oracle_channel.restype = None
+    lib.sscan_oracle_fwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, ci, dp, dp, dp,
+                                        i64, i64, i64, i64, ci, ci]
+    lib.sscan_oracle_fwd_ex.restype = ci
+    lib.sscan_oracle_channel_ex.argtypes = [vp, vp, vp, i64, fp, vp, vp, fp, fp, ci, fp, ci,
+                                            i64, i64, ci, dp, i64, dp, dp]
+    lib.sscan_oracle_channel_ex.restype = None
     _lib_cache[path] = lib
     return lib
 
@@ -80,11 +86,14 @@ def _ptr(a: Optional[np.ndarray]):
 
 
 def fwd(u, delta, A, B, C, Dskip=None, z=None, delta_bias=None, softplus: bool = True,
-        io: str = "f32", threads: Optional[int] = None, want_mag: bool = False, lib=None):
+        io: str = "f32", threads: Optional[int] = None, want_mag: bool = False, lib=None,
+        h0=None, euler: bool = False):
     """Selective-scan forward over whole tensors.
 
     u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) float32; Dskip, delta_bias:
-    (dim,) float32. For ``io="bf16"`` the io tensors are uint16 arrays holding bf16 bit patterns.
+    (dim,) float32; h0: (batch, dim, N) float32 initial state or None for zero; ``euler``
+    selects the first-order factor ``1 + dt A`` instead of ``exp(dt A)``. For ``io="bf16"`` the
+    io tensors are uint16 arrays holding bf16 bit patterns.
     Returns ``(y, h_last)`` as float64 arrays of shapes (batch, L, dim) and (batch, dim, N), plus
     the absolute-value magnitude of every output when ``want_mag``.
     """
@@ -100,23 +109,30 @@ def fwd(u, delta, A, B, C, Dskip=None, z=None, delta_bias=None, softplus: bool =
     assert A.shape == (dim, N)
     Dskip = None if Dskip is None else np.ascontiguousarray(Dskip, dtype=np.float32)
     delta_bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    if h0 is not None:
+        if h0.dtype != np.float32 or h0.shape != (batch, dim, N):
+            raise TypeError(f"h0 must be float32 of shape {(batch, dim, N)}")
+        h0 = np.ascontiguousarray(h0)
     y = np.empty((batch, L, dim), dtype=np.float64)
     h = np.empty((batch, dim, N), dtype=np.float64)
     mag = np.empty_like(y) if want_mag else None
     nt = threads or os.cpu_count() or 1
-    rc = lib.sscan_oracle_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
-                              _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h),
-                              _ptr(mag), batch, L, dim, N, int(io == "bf16"), int(nt))
+    rc = lib.sscan_oracle_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                                 _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                                 int(bool(euler)), _ptr(y), _ptr(h), _ptr(mag), batch, L, dim, N,
+                                 int(io == "bf16"), int(nt))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     return (y, h, mag) if want_mag else (y, h)
 
 
 def fwd_channel(u, delta, A_d, B, C, Dskip_d=None, z=None, bias_d=None, softplus: bool = True,
-                io: str = "f32", want_mag: bool = False, lib=None):
+                io: str = "f32", want_mag: bool = False, lib=None, h0_d=None,
+                euler: bool = False):
     """One channel: u, delta, z are (L,) io arrays, B and C (L, N), A_d (N,) float32, Dskip_d and
-    bias_d Python floats (stored as float32) or None. Returns ``(y (L,), h_last (N,))`` in float64
-    (plus the magnitude when ``want_mag``). Used to check sampled channels of large runs."""
+    bias_d Python floats (stored as float32) or None, h0_d (N,) float32 or None. Returns
+    ``(y (L,), h_last (N,))`` in float64 (plus the magnitude when ``want_mag``). Used to check
+    sampled channels of large runs."""
     lib = lib or load()
     u, delta = _io_array(u, io), _io_array(delta, io)
     B, C = _io_array(B, io), _io_array(C, io)
@@ -129,7 +145,9 @@ def fwd_channel(u, delta, A_d, B, C, Dskip_d=None, z=None, bias_d=None, softplus
     y = np.empty(L, dtype=np.float64)
     h = np.empty(N, dtype=np.float64)
     mag = np.empty(L, dtype=np.float64) if want_mag else None
-    lib.sscan_oracle_channel(_ptr(u), _ptr(delta), _ptr(z), 1, _ptr(A_d), _ptr(B), _ptr(C),
-                             _ptr(Dv), _ptr(bv), int(bool(softplus)), L, N, int(io == "bf16"),
-                             _ptr(y), 1, _ptr(h), _ptr(mag))
+    h0v = None if h0_d is None else np.ascontiguousarray(h0_d, dtype=np.float32)
+    lib.sscan_oracle_channel_ex(_ptr(u), _ptr(delta), _ptr(z), 1, _ptr(A_d), _ptr(B), _ptr(C),
+                                _ptr(Dv), _ptr(bv), int(bool(softplus)), _ptr(h0v),
+                                int(bool(euler)), L, N, int(io == "bf16"), _ptr(y), 1, _ptr(h),
+                                _ptr(mag))
     return (y, h, mag) if want_mag else (y, h)

@@ -457,7 +457,10 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
       for (int t = 0; t < TC; ++t) {
         const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
         const float4* Cq = reinterpret_cast<const float4*>(Cs + t * kNP + n0);
-        float2 acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+        constexpr int NACC = KP < 4 ? KP : 4;  // independent partial sums of the readout
+        float2 acc[NACC];
+#pragma unroll
+        for (int i = 0; i < NACC; ++i) acc[i] = f2(0.f, 0.f);
 #pragma unroll
         for (int qq = 0; qq < K / 4; ++qq) {
           const float4 bq = Bq[qq], cq = Cq[qq];
@@ -469,10 +472,14 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
             h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
-            acc[r & 3] = __ffma2_rn(cc, h[r], acc[r & 3]);
+            acc[r % NACC] = __ffma2_rn(cc, h[r], acc[r % NACC]);
           }
         }
-        const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        float2 a2;
+        if constexpr (NACC == 4)
+          a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        else
+          a2 = __fadd2_rn(acc[0], acc[1]);
         ys[t] = a2.x + a2.y;
       }
 
@@ -775,7 +782,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
 cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
   // Layout from the number of channels (batch x dim), measured on B300: one lane per channel
   // (16 states per lane, 256-thread CTAs) from about 24k channels up; two lanes (128 threads)
-  // from about 16k; four lanes (64 threads) below that. When the sequence will be split into
+  // from about 16k; four lanes (128 threads) below that. When the sequence will be split into
   // time segments anyway (too few warps even with four lanes), one lane per channel again.
   const int64_t chans = a.batch * a.dim;
   int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
@@ -783,7 +790,7 @@ cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
     G = chans >= 24576 ? 1 : (chans >= 16384 ? 2 : 4);
     if (chans * 4 / 32 < kSplitBelowWarps) G = 1;
   }
-  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
+  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : 128);
   if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;

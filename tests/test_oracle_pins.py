@@ -324,8 +324,119 @@ def pin_bf16_widening(lib=None):
     assert _bf16_to_f32(np.array([0x3FC0, 0xC040], np.uint16)).tolist() == [1.5, -3.0]
 
 
+# ---------------------------------------------------------------------------------------------
+# 9. Initial state h0 (recurrent mode: the state is all that carries from one step to the next,
+#    "Mamba：选择性状态空间模型入门教程", "Mamba 的关键创新：选择性机制").
+# ---------------------------------------------------------------------------------------------
+def _h0_inputs(rng, batch, L, dim, N):
+    u, z = (_f32(rng.standard_normal((batch, L, dim))) for _ in range(2))
+    delta = _f32(rng.standard_normal((batch, L, dim)))
+    Bm, Cm = (_f32(rng.standard_normal((batch, L, N))) for _ in range(2))
+    A = _f32(-np.exp(rng.uniform(0, math.log(8), (dim, N))))
+    Dskip = _f32(rng.standard_normal(dim))
+    bias = _f32(rng.uniform(-3, -1, dim))
+    h0 = _f32(rng.standard_normal((batch, dim, N)))
+    return u, delta, A, Bm, Cm, Dskip, z, bias, h0
+
+
+def pin_h0_free_decay(lib=None):
+    """u = 0: no input enters, so h_t = exp(A sum_{s<=t} dt_s) h0 (one exponential of the summed
+    steps) and y_t = (C_t . h_t) SiLU(z_t)."""
+    rng = np.random.default_rng(21)
+    batch, L, dim, N = 2, 24, 3, 6
+    u, delta, A, Bm, Cm, Dskip, z, bias, h0 = _h0_inputs(rng, batch, L, dim, N)
+    u0 = np.zeros_like(u)
+    y, h = oracle.fwd(u0, delta, A, Bm, Cm, Dskip, z, bias, softplus=True, lib=lib, h0=h0)
+    dt = np.logaddexp(0.0, delta.astype(np.float64) + bias.astype(np.float64))  # (batch, L, dim)
+    cum = np.cumsum(dt, axis=1)
+    for b in range(batch):
+        for d in range(dim):
+            ht = np.exp(cum[b, :, d, None] * A[d].astype(np.float64)[None, :]) \
+                * h0[b, d].astype(np.float64)[None, :]                     # (L, N)
+            zz = z[b, :, d].astype(np.float64)
+            ref = np.einsum("tn,tn->t", Cm[b].astype(np.float64), ht) * zz * expit(zz)
+            np.testing.assert_allclose(y[b, :, d], ref, rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(h[b, d], ht[-1], rtol=1e-12, atol=1e-15)
+    # First-order factor: h_t = prod_{s<=t} (1 + dt_s A) h0, with steps small enough to decay.
+    bs = _f32(bias - 3.0)
+    y, h = oracle.fwd(u0, delta, A, Bm, Cm, Dskip, z, bs, softplus=True, lib=lib, h0=h0,
+                      euler=True)
+    dt = np.logaddexp(0.0, delta.astype(np.float64) + bs.astype(np.float64))
+    for b in range(batch):
+        for d in range(dim):
+            fac = 1.0 + dt[b, :, d, None] * A[d].astype(np.float64)[None, :]   # (L, N)
+            ht = np.cumprod(fac, axis=0) * h0[b, d].astype(np.float64)[None, :]
+            zz = z[b, :, d].astype(np.float64)
+            ref = np.einsum("tn,tn->t", Cm[b].astype(np.float64), ht) * zz * expit(zz)
+            np.testing.assert_allclose(y[b, :, d], ref, rtol=1e-11, atol=1e-13)
+
+
+def pin_h0_superposition(lib=None):
+    """The scan is linear in (h0, inputs) for fixed steps: y(h0, u) = y(0, u) + y(h0, u = 0)."""
+    rng = np.random.default_rng(22)
+    batch, L, dim, N = 2, 30, 4, 5
+    u, delta, A, Bm, Cm, Dskip, z, bias, h0 = _h0_inputs(rng, batch, L, dim, N)
+    y1, h1 = oracle.fwd(u, delta, A, Bm, Cm, Dskip, z, bias, lib=lib, h0=h0)
+    y2, h2 = oracle.fwd(u, delta, A, Bm, Cm, Dskip, z, bias, lib=lib)
+    y3, h3 = oracle.fwd(np.zeros_like(u), delta, A, Bm, Cm, Dskip, z, bias, lib=lib, h0=h0)
+    scale = np.abs(y2).max() + np.abs(y3).max()
+    np.testing.assert_allclose(y1, y2 + y3, rtol=0, atol=1e-13 * scale)
+    np.testing.assert_allclose(h1, h2 + h3, rtol=0, atol=1e-13 * (np.abs(h2).max() + np.abs(h3).max()))
+
+
+def pin_h0_split_sequence(lib=None):
+    """Running steps [0, L1) and then [L1, L) from the carried state equals one run over [0, L)
+    (the carried state rounded to fp32 on the way, as the library's h_last / h0 are)."""
+    rng = np.random.default_rng(23)
+    batch, L, dim, N, L1 = 2, 40, 3, 7, 17
+    u, delta, A, Bm, Cm, Dskip, z, bias, _ = _h0_inputs(rng, batch, L, dim, N)
+    for euler in (False, True):
+        # Euler is stable only for dt |A| < 2: give it smaller steps.
+        bs = _f32(bias - 3.0) if euler else bias
+        y, h = oracle.fwd(u, delta, A, Bm, Cm, Dskip, z, bs, lib=lib, euler=euler)
+        ya, ha = oracle.fwd(u[:, :L1].copy(), delta[:, :L1].copy(), A, Bm[:, :L1].copy(),
+                            Cm[:, :L1].copy(), Dskip, z[:, :L1].copy(), bs, lib=lib, euler=euler)
+        yb, hb = oracle.fwd(u[:, L1:].copy(), delta[:, L1:].copy(), A, Bm[:, L1:].copy(),
+                            Cm[:, L1:].copy(), Dskip, z[:, L1:].copy(), bs, lib=lib,
+                            h0=ha.astype(np.float32), euler=euler)
+        np.testing.assert_array_equal(ya, y[:, :L1])
+        scale = np.abs(y).max()
+        np.testing.assert_allclose(yb, y[:, L1:], rtol=0, atol=1e-6 * scale)
+        np.testing.assert_allclose(hb, h, rtol=0, atol=1e-6 * np.abs(h).max())
+
+
+# ---------------------------------------------------------------------------------------------
+# 10. First-order (Euler) decay factor 1 + dt A: with constant dt, B, C the recurrence unrolls
+#     into a causal convolution with K[k] = sum_n C dt B (1 + dt A)^k ("架构变体：Mamba/SSM",
+#     "并行卷积"; the factor is the first-order expansion of exp(dt A), "从RNN到Mamba" 3.2).
+# ---------------------------------------------------------------------------------------------
+def pin_euler_lti(lib=None):
+    rng = np.random.default_rng(12)
+    batch, L, dim, N = 2, 36, 3, 4
+    u = _f32(rng.standard_normal((batch, L, dim)))
+    A = _f32(-np.exp(rng.uniform(0, math.log(8), (dim, N))))
+    Bv = _f32(rng.standard_normal((batch, N)))
+    Cv = _f32(rng.standard_normal((batch, N)))
+    Dskip = _f32(rng.standard_normal(dim))
+    delta = _f32(np.broadcast_to(rng.uniform(0.01, 0.1, (1, 1, dim)), (batch, L, dim)))
+    Bm = _f32(np.broadcast_to(Bv[:, None, :], (batch, L, N)))
+    Cm = _f32(np.broadcast_to(Cv[:, None, :], (batch, L, N)))
+    y, h = oracle.fwd(u, delta, A, Bm, Cm, Dskip, None, None, softplus=False, lib=lib, euler=True)
+    dt = delta[0, 0].astype(np.float64)
+    k = np.arange(L)
+    for b in range(batch):
+        for d in range(dim):
+            K = np.zeros(L)
+            for n in range(N):
+                K += float(Cv[b, n]) * dt[d] * float(Bv[b, n]) * (1.0 + dt[d] * float(A[d, n])) ** k
+            uu = u[b, :, d].astype(np.float64)
+            ref = np.convolve(K, uu)[:L] + float(Dskip[d]) * uu
+            np.testing.assert_allclose(y[b, :, d], ref, rtol=1e-11, atol=1e-13)
+
+
 PINS = [pin_worked_example, pin_selective_demo, pin_lti_convolution, pin_matrix_form,
-        pin_associativity, pin_delta_zero, pin_skip_gate, pin_softplus, pin_bf16_widening]
+        pin_associativity, pin_delta_zero, pin_skip_gate, pin_softplus, pin_bf16_widening,
+        pin_h0_free_decay, pin_h0_superposition, pin_h0_split_sequence, pin_euler_lti]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -362,6 +473,9 @@ MUTANTS = {
     9: "Euler step instead of zero-order hold",
     10: "B and C swapped",
     11: "B/C rows taken from another batch",
+    12: "initial state ignored",
+    13: "initial state not decayed at the first step",
+    14: "Euler factor with the page's sign (1 - dt A)",
 }
 
 
