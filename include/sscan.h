@@ -28,6 +28,12 @@ extern "C" {
 
 typedef enum { SSCAN_F32 = 0, SSCAN_BF16 = 1 } sscan_dtype_t;
 
+/* Decay factor of one step. ZOH: exp(dt * A), the zero-order hold of "架构变体：Mamba/SSM",
+ * section "离散化". EULER: 1 + dt * A, the first-order expansion of exp(dt * A) (section 3.2 of
+ * "从RNN到Mamba：深入浅出图解'选择性状态空间'如何让模型学会'忘记'" prints it as (I - Delta A),
+ * which grows without bound for A < 0; the sign is read as +). EULER is stable for dt |A| < 2. */
+typedef enum { SSCAN_DISC_ZOH = 0, SSCAN_DISC_EULER = 1 } sscan_disc_t;
+
 typedef enum {
   SSCAN_OK = 0,
   SSCAN_ERR_INVALID_ARG = 1,   /* null required pointer, negative size, N outside 1..16, ... */
@@ -69,6 +75,47 @@ sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const
                          const void* C, const float* D, const void* z, const float* delta_bias,
                          int softplus_flag, void* y, float* h_last, int64_t batch, int64_t L,
                          int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * sscan_fwd_ex -- sscan_fwd from a given initial state, with a choice of decay factor.
+ *
+ * The recurrent (step-by-step) mode of the scan carries nothing but the state from one step to
+ * the next ("Mamba：选择性状态空间模型入门教程", "Mamba 的关键创新：选择性机制"; "Mamba:
+ * Linear-Time Sequence Modeling with Selective State Spaces", "核心贡献：选择机制（S6）"), so a
+ * sequence can be processed in pieces: pass one call's h_last as the next call's h0.
+ *
+ *   h0   : (batch, dim, N) fp32 device memory, the state before step 0, or NULL for zero. It may
+ *          be the same buffer as h_last: every thread block reads its part of h0 before any
+ *          part of h_last is written, so a sequence can be continued in place.
+ *   disc : SSCAN_DISC_ZOH (what sscan_fwd computes) or SSCAN_DISC_EULER.
+ * Everything else is as for sscan_fwd; L = 0 copies h0 (or zero) to h_last. An out-of-range
+ * disc returns SSCAN_ERR_INVALID_ARG.
+ */
+sscan_status_t sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z,
+                            const float* delta_bias, int softplus_flag, const float* h0,
+                            sscan_disc_t disc, void* y, float* h_last, int64_t batch, int64_t L,
+                            int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * sscan_step -- one step of the recurrence for every (batch, channel): recurrent inference
+ * (decoding), constant work per token ("Mamba：选择性状态空间模型入门教程", recurrent mode at
+ * inference time; "Mamba: Linear-Time Sequence Modeling with Selective State Spaces", constant
+ * memory per generated token).
+ *
+ *   u, delta, z : (batch, dim) this step's inputs, element type `dtype` (z nullable)
+ *   B, C        : (batch, N), element type `dtype`
+ *   A (dim, N), D (dim), delta_bias (dim): fp32 as for sscan_fwd (D, delta_bias nullable)
+ *   h           : (batch, dim, N) fp32 device state, read and overwritten with the new state
+ *   y           : (batch, dim) output, element type `dtype`
+ * Computes exactly one step of sscan_fwd_ex (same dt, decay factor, skip and gate), so a prefill
+ * by sscan_fwd_ex followed by steps from its h_last continues the same sequence. Asynchronous
+ * on `stream`; allocates nothing; argument errors as for sscan_fwd (h must not be NULL).
+ */
+sscan_status_t sscan_step(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, sscan_disc_t disc, float* h, void* y, int64_t batch,
+                          int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
 
 /*
  * sscan_fwd_host -- the same operation on HOST buffers: copies the inputs to the current

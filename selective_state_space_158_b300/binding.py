@@ -17,6 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libsscan.so")
 
 SSCAN_F32, SSCAN_BF16 = 0, 1
+SSCAN_DISC_ZOH, SSCAN_DISC_EULER = 0, 1
 STATUS = {0: "SSCAN_OK", 1: "SSCAN_ERR_INVALID_ARG", 2: "SSCAN_ERR_UNSUPPORTED",
           3: "SSCAN_ERR_CUDA", 4: "SSCAN_ERR_CARRY_TIMEOUT", 5: "SSCAN_ERR_SCRATCH_TOO_SMALL"}
 
@@ -24,8 +25,16 @@ STATUS = {0: "SSCAN_OK", 1: "SSCAN_ERR_INVALID_ARG", 2: "SSCAN_ERR_UNSUPPORTED",
 _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i64, _i64, _i64,
              _int, _vp]
+# sscan_fwd_ex: sscan_fwd's arguments with h0 and disc inserted after softplus_flag.
+_FWD_EX_ARGS = _FWD_ARGS[:9] + [_vp, _int] + _FWD_ARGS[9:]
+# sscan_step: u, delta, A, B, C, D, z, delta_bias, softplus, disc, h, y, batch, dim, N, dtype,
+# stream.
+_STEP_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp, _vp, _i64, _i64, _i64,
+              _int, _vp]
 SIGNATURES = {
     "sscan_fwd": (_FWD_ARGS, _int),
+    "sscan_fwd_ex": (_FWD_EX_ARGS, _int),
+    "sscan_step": (_STEP_ARGS, _int),
     "sscan_fwd_host": (_FWD_ARGS, _int),
     "sscan_fwd_noalloc": (_FWD_ARGS, _int),
     "sscan_get_device_error": ([_vp], _int),
@@ -86,11 +95,14 @@ def fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
         C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
         delta_bias: Optional[torch.Tensor] = None, softplus: bool = True,
         y: Optional[torch.Tensor] = None, h_last: Optional[torch.Tensor] = None,
-        return_last_state: bool = True, stream=None):
+        return_last_state: bool = True, stream=None, h0: Optional[torch.Tensor] = None,
+        euler: bool = False):
     """Selective-scan forward on CUDA tensors (asynchronous on ``stream`` or the current stream).
 
     u, delta, z: (batch, L, dim); B, C: (batch, L, N) with 1 <= N <= 16, all of one io dtype
-    (float32 or bfloat16); A: (dim, N) float32; D, delta_bias: (dim,) float32.
+    (float32 or bfloat16); A: (dim, N) float32; D, delta_bias: (dim,) float32; h0: optional
+    initial state (batch, dim, N) float32; ``euler`` selects the decay factor 1 + dt A.
+    Calls ``sscan_fwd``, or ``sscan_fwd_ex`` when h0 or euler is given.
     Returns ``y`` (batch, L, dim) in the io dtype and, if ``return_last_state``, ``h_last``
     (batch, dim, N) float32.
     """
@@ -108,10 +120,11 @@ def fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
             raise ValueError(f"{name}: expected {shape} {dt} on {dev}, got "
                              f"{tuple(t.shape)} {t.dtype} on {t.device}")
     for name, t, shape, dt in [("D", D, (dim,), torch.float32), ("z", z, (batch, L, dim), u.dtype),
-                               ("delta_bias", delta_bias, (dim,), torch.float32)]:
+                               ("delta_bias", delta_bias, (dim,), torch.float32),
+                               ("h0", h0, (batch, dim, N), torch.float32)]:
         if t is not None and (tuple(t.shape) != shape or t.dtype != dt or t.device != dev):
             raise ValueError(f"{name}: expected {shape} {dt} on {dev}")
-    ts = [u, delta, A, B, C, D, z, delta_bias]
+    ts = [u, delta, A, B, C, D, z, delta_bias, h0]
     if any(t is not None and not t.is_contiguous() for t in ts):
         raise ValueError("all tensors must be contiguous")
     if y is None:
@@ -119,11 +132,61 @@ def fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
     if return_last_state and h_last is None:
         h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
-        code = lib.sscan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                             _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),
-                             batch, L, dim, N, io, _stream_handle(stream, dev))
-    _check(code, "sscan_fwd")
+        if h0 is None and not euler:
+            where = "sscan_fwd"
+            code = lib.sscan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y),
+                                 _ptr(h_last), batch, L, dim, N, io, _stream_handle(stream, dev))
+        else:
+            where = "sscan_fwd_ex"
+            code = lib.sscan_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                                    SSCAN_DISC_EULER if euler else SSCAN_DISC_ZOH, _ptr(y),
+                                    _ptr(h_last), batch, L, dim, N, io,
+                                    _stream_handle(stream, dev))
+    _check(code, where)
     return (y, h_last) if return_last_state else y
+
+
+def step(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+         C: torch.Tensor, h: torch.Tensor, D: Optional[torch.Tensor] = None,
+         z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+         softplus: bool = True, euler: bool = False, y: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """One recurrence step for every (batch, channel) through ``sscan_step``.
+
+    u, delta, z: (batch, dim); B, C: (batch, N), one io dtype; A: (dim, N) float32; h: (batch,
+    dim, N) float32 state, updated in place. Returns y (batch, dim) in the io dtype.
+    """
+    lib = load()
+    io = _dtype_code(u)
+    batch, dim = u.shape
+    N = B.shape[-1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("libsscan computes on CUDA tensors only")
+    for name, t, shape, dt in [("delta", delta, (batch, dim), u.dtype),
+                               ("B", B, (batch, N), u.dtype), ("C", C, (batch, N), u.dtype),
+                               ("A", A, (dim, N), torch.float32),
+                               ("h", h, (batch, dim, N), torch.float32)]:
+        if tuple(t.shape) != shape or t.dtype != dt or t.device != dev:
+            raise ValueError(f"{name}: expected {shape} {dt} on {dev}")
+    for name, t, shape, dt in [("D", D, (dim,), torch.float32), ("z", z, (batch, dim), u.dtype),
+                               ("delta_bias", delta_bias, (dim,), torch.float32)]:
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dt or t.device != dev):
+            raise ValueError(f"{name}: expected {shape} {dt} on {dev}")
+    if any(t is not None and not t.is_contiguous() for t in [u, delta, A, B, C, h, D, z,
+                                                              delta_bias]):
+        raise ValueError("all tensors must be contiguous")
+    if y is None:
+        y = torch.empty_like(u)
+    with torch.cuda.device(dev):
+        code = lib.sscan_step(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                              _ptr(delta_bias), int(bool(softplus)),
+                              SSCAN_DISC_EULER if euler else SSCAN_DISC_ZOH, _ptr(h), _ptr(y),
+                              batch, dim, N, io, _stream_handle(stream, dev))
+    _check(code, "sscan_step")
+    return y
 
 
 def fwd_host(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

@@ -96,19 +96,22 @@ const char* sscan_status_string(sscan_status_t s) {
   return "SSCAN_ERR_UNKNOWN";
 }
 
-sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                         const void* C, const float* D, const void* z, const float* delta_bias,
-                         int softplus_flag, void* y, float* h_last, int64_t batch, int64_t L,
-                         int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream) {
+sscan_status_t sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z,
+                            const float* delta_bias, int softplus_flag, const float* h0,
+                            sscan_disc_t disc, void* y, float* h_last, int64_t batch, int64_t L,
+                            int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream) {
   int64_t bld = 0, bln = 0;
+  if (disc != SSCAN_DISC_ZOH && disc != SSCAN_DISC_EULER) return SSCAN_ERR_INVALID_ARG;
   sscan_status_t st = check_args(u, delta, A, B, C, y, batch, L, dim, N, dtype, &bld, &bln);
   if (st != SSCAN_OK) return st;
   const int dev = current_device();
   if (dev < 0) return SSCAN_ERR_CUDA;
   if (batch == 0 || dim == 0) return SSCAN_OK;
-  if (L == 0) {
-    if (h_last &&
-        cudaMemsetAsync(h_last, 0, size_t(batch * dim * N) * sizeof(float), stream) != cudaSuccess)
+  if (L == 0) {  // the final state is the initial state
+    const size_t hb = size_t(batch * dim * N) * sizeof(float);
+    if (h_last && (h0 ? cudaMemcpyAsync(h_last, h0, hb, cudaMemcpyDeviceToDevice, stream)
+                      : cudaMemsetAsync(h_last, 0, hb, stream)) != cudaSuccess)
       return SSCAN_ERR_CUDA;
     return SSCAN_OK;
   }
@@ -122,6 +125,8 @@ sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const
   a.z = z;
   a.bias = delta_bias;
   a.softplus = softplus_flag != 0;
+  a.h0 = h0;
+  a.euler = disc == SSCAN_DISC_EULER;
   a.y = y;
   a.h_last = h_last;
   a.batch = batch;
@@ -140,6 +145,48 @@ sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const
   else
     e = sscan::launch_simple(a);
   return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
+sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus_flag, void* y, float* h_last, int64_t batch, int64_t L,
+                         int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream) {
+  return sscan_fwd_ex(u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr,
+                      SSCAN_DISC_ZOH, y, h_last, batch, L, dim, N, dtype, stream);
+}
+
+sscan_status_t sscan_step(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, sscan_disc_t disc, float* h, void* y, int64_t batch,
+                          int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream) {
+  if (disc != SSCAN_DISC_ZOH && disc != SSCAN_DISC_EULER) return SSCAN_ERR_INVALID_ARG;
+  int64_t bld = 0, bln = 0;
+  sscan_status_t st = check_args(u, delta, A, B, C, y, batch, 1, dim, N, dtype, &bld, &bln);
+  if (st != SSCAN_OK) return st;
+  if (batch * dim > 0 && !h) return SSCAN_ERR_INVALID_ARG;
+  if (current_device() < 0) return SSCAN_ERR_CUDA;
+  if (batch == 0 || dim == 0) return SSCAN_OK;
+  sscan::FwdArgs a;
+  a.u = u;
+  a.delta = delta;
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.D = D;
+  a.z = z;
+  a.bias = delta_bias;
+  a.softplus = softplus_flag != 0;
+  a.euler = disc == SSCAN_DISC_EULER;
+  a.y = y;
+  a.h_last = h;  // read and written in place
+  a.batch = batch;
+  a.L = 1;
+  a.dim = dim;
+  a.N = N;
+  a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
+  a.stream = stream;
+  a.status = nullptr;
+  return sscan::launch_step(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 
 sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, const void* B,

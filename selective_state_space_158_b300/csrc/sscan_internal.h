@@ -21,6 +21,8 @@ struct FwdArgs {
   const void* z;        // nullable
   const float* bias;    // nullable
   int softplus;
+  const float* h0 = nullptr;  // initial state (batch, dim, N) fp32, nullable
+  int euler = 0;              // decay factor 1 + dt A instead of exp(dt A)
   void* y;
   float* h_last;        // nullable
   int64_t batch, L, dim, N;
@@ -58,6 +60,8 @@ bool tma_path_ok(const FwdArgs& a);
 cudaError_t launch_simple(const FwdArgs& a);
 cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& t);
 cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& t);
+// One step of the recurrence for every (batch, channel); h_last is the state, read and written.
+cudaError_t launch_step(const FwdArgs& a);
 
 // Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS from the environment (0: unset).
 TmaTuning tuning_from_env();

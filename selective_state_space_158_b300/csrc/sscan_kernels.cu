@@ -36,20 +36,21 @@ constexpr unsigned kErrTimeout = 1u << 4;  // status bit: a bounded wait ran out
 // ================================================================================================
 // Plain-load kernel: one thread per (batch row, channel), states in registers, sequential in t.
 // ================================================================================================
-template <typename IO>
+template <typename IO, bool EULER>
 __global__ void __launch_bounds__(128) sscan_simple_kernel(
     const IO* __restrict__ u, const IO* __restrict__ delta, const float* __restrict__ A,
     const IO* __restrict__ Bm, const IO* __restrict__ Cm, const float* __restrict__ Dskip,
-    const IO* __restrict__ z, const float* __restrict__ bias, int softplus, IO* __restrict__ y,
-    float* __restrict__ h_last, int64_t batch, int64_t L, int64_t dim, int N) {
+    const IO* __restrict__ z, const float* __restrict__ bias, int softplus,
+    const float* __restrict__ h0, IO* __restrict__ y, float* __restrict__ h_last, int64_t batch,
+    int64_t L, int64_t dim, int N) {
   const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= batch * dim) return;
   const int64_t b = c / dim, d = c - b * dim;
   float A2[kNP], h[kNP];
 #pragma unroll
   for (int n = 0; n < kNP; ++n) {
-    A2[n] = n < N ? A[d * N + n] * kLog2e : 0.f;
-    h[n] = 0.f;
+    A2[n] = n < N ? A[d * N + n] * (EULER ? 1.f : kLog2e) : 0.f;
+    h[n] = (h0 && n < N) ? h0[c * N + n] : 0.f;
   }
   const float bs = bias ? bias[d] : 0.f;
   const float Dd = Dskip ? Dskip[d] : 0.f;
@@ -65,7 +66,7 @@ __global__ void __launch_bounds__(128) sscan_simple_kernel(
 #pragma unroll
     for (int n = 0; n < kNP; ++n) {
       if (n < N) {
-        const float e = ex2(fmaf(dt, A2[n], kEx2ArgShift));
+        const float e = EULER ? fmaf(dt, A2[n], 1.f) : ex2(fmaf(dt, A2[n], kEx2ArgShift));
         h[n] = fmaf(e, h[n], dtu * to_f32(Bt[n]));
         acc = fmaf(to_f32(Ct[n]), h[n], acc);
       }
@@ -110,6 +111,7 @@ struct LaneParams {
   const float* A;
   const float* D;
   const float* bias;
+  const float* h0;       // initial state (batch, dim, N), or null for zero
   float* h_last;
   unsigned int* status;
   int L, dim, N, batch;
@@ -122,7 +124,7 @@ struct LaneParams {
   // chunk-carry workspace (n_seg > 1)
   unsigned int* ticket;  // zero at launch
   unsigned int* flags;   // [n_seg][batch][n_cg][W] warp units
-  float* agg;            // [unit][lane][K + 1]: H then SD
+  float* agg;            // [unit][lane][2K]: H, then SD (zero-order hold) or P (first order)
   int skip_publish;      // test hook: this segment never publishes (-1: off)
 };
 
@@ -202,7 +204,7 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_shared(unsigned* p, unsigne
 template <int G>
 __host__ __device__ constexpr int lane_min_blocks() { return G == 4 ? 2 : 1; }
 
-template <typename IO, int G, int TC>
+template <typename IO, int G, int TC, bool EULER>
 __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -213,6 +215,16 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
   constexpr int CPW = 32 / G;    // channels per warp
   static_assert(G == 1 || G == 2 || G == 4, "G must be 1, 2 or 4");
   static_assert(TC % 2 == 0, "chunk must be even");
+  // Decay factor of one step: 2^(dt * A log2e) on the SFU (zero-order hold), or 1 + dt * A (first
+  // order). A2 holds A log2e or A accordingly; kArg is the addend of the FMA.
+  constexpr float kScaleA = EULER ? 1.f : kLog2e;
+  constexpr float kArg = EULER ? 1.f : kEx2ArgShift;
+  auto decay = [](float2 arg) -> float2 {
+    if constexpr (EULER)
+      return arg;
+    else
+      return f2(ex2(arg.x), ex2(arg.y));
+  };
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
 
@@ -303,14 +315,22 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
   const int n0 = g * K;
   const int cg = ch0 + cl;               // global channel
   const bool live = cg < p.dim;
-  float2 A2[KP], h[KP];
+  float2 A2[KP], h[KP], hz[KP];
+  // The initial state, read once before anything is written (so h0 may alias h_last). It
+  // enters the first pass directly when the sequence is not split, and through the fold of
+  // predecessor aggregates below when it is.
+  const float* h0c = (p.h0 && live) ? p.h0 + (size_t(b) * p.dim + cg) * N : nullptr;
 #pragma unroll
   for (int r = 0; r < KP; ++r) {
     const int n = n0 + 2 * r;
-    A2[r] = f2((live && n < N) ? p.A[size_t(cg) * N + n] * kLog2e : 0.f,
-               (live && n + 1 < N) ? p.A[size_t(cg) * N + n + 1] * kLog2e : 0.f);
-    h[r] = f2(0.f, 0.f);
+    A2[r] = f2((live && n < N) ? p.A[size_t(cg) * N + n] * kScaleA : 0.f,
+               (live && n + 1 < N) ? p.A[size_t(cg) * N + n + 1] * kScaleA : 0.f);
+    hz[r] = f2((h0c && n < N) ? h0c[n] : 0.f, (h0c && n + 1 < N) ? h0c[n + 1] : 0.f);
+    h[r] = p.n_seg == 1 ? hz[r] : f2(0.f, 0.f);
   }
+  float2 Pr[EULER ? KP : 1];  // first order: product of this segment's decay factors (pass 1)
+#pragma unroll
+  for (int r = 0; r < (EULER ? KP : 1); ++r) Pr[r] = f2(1.f, 1.f);
   const float bias_c = (p.bias && live) ? p.bias[cg] : 0.f;
   const float D_c = (p.D && live) ? p.D[cg] : 0.f;
   IO* ywarp0 = reinterpret_cast<IO*>(smem + lay.off_y) + size_t(warp) * (lay.y_warp / sizeof(IO));
@@ -325,11 +345,16 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
     const bool readout = pass == 1;
     if (readout && p.n_seg > 1) {
       // Start state of this segment: predecessors' aggregates folded from the nearest back to
-      // segment 0 (later o earlier), always in that order, so the result is deterministic.
-      // (Segment 0 starts from zero; pass 1 left its aggregate in h.)
-      float2 accH[KP];
+      // segment 0 (later o earlier), always in that order, so the result is deterministic;
+      // then the initial state decayed over all of them. (Segment 0 starts from h0 or zero;
+      // pass 1 left its aggregate in h.) accP is the decay accumulated so far: 2^(A2 acc_sd)
+      // for zero-order hold, the running product of the segments' P for first order.
+      float2 accH[KP], accP[KP];
 #pragma unroll
-      for (int r = 0; r < KP; ++r) accH[r] = f2(0.f, 0.f);
+      for (int r = 0; r < KP; ++r) {
+        accH[r] = f2(0.f, 0.f);
+        accP[r] = f2(1.f, 1.f);
+      }
       float acc_sd = 0.f;
       for (int j = seg - 1; j >= 0; --j) {
         const size_t uj = unit - size_t(seg - j) * units_per_seg;
@@ -345,16 +370,21 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
         f = __shfl_sync(0xffffffffu, f, 0);
         __syncwarp();
         if (f == 0) continue;  // timed out: the status word says so; skip this aggregate
-        const float* a = p.agg + (uj * 32 + lane) * (K + 1);
+        const float* a = p.agg + (uj * 32 + lane) * (2 * K);
 #pragma unroll
         for (int r = 0; r < KP; ++r) {  // acc <- acc o agg_j: agg_j's end state decays over acc
-          const float2 dec = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
-          accH[r] = __ffma2_rn(dec, f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
+          if constexpr (!EULER) accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+          accH[r] = __ffma2_rn(accP[r], f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
+          if constexpr (EULER)
+            accP[r] = __fmul2_rn(accP[r], f2(__ldcg(a + K + 2 * r), __ldcg(a + K + 2 * r + 1)));
         }
-        acc_sd += __ldcg(a + K);
+        if constexpr (!EULER) acc_sd += __ldcg(a + K);
       }
 #pragma unroll
-      for (int r = 0; r < KP; ++r) h[r] = accH[r];
+      for (int r = 0; r < KP; ++r) {
+        if constexpr (!EULER) accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+        h[r] = __ffma2_rn(accP[r], hz[r], accH[r]);
+      }
     }
     for (int ci = 0; ci < nch; ++ci, ++q) {
       const int c = c_begin + ci;
@@ -435,10 +465,10 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int r = 2 * qq + j;
-              const float2 arg = __ffma2_rn(dtp[t], A2[r], f2(kEx2ArgShift, kEx2ArgShift));
-              const float2 dA = f2(ex2(arg.x), ex2(arg.y));
+              const float2 dA = decay(__ffma2_rn(dtp[t], A2[r], f2(kArg, kArg)));
               const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
               h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
+              if constexpr (EULER) Pr[r] = __fmul2_rn(Pr[r], dA);
             }
           }
         }
@@ -467,8 +497,7 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int r = 2 * qq + j;
-            const float2 arg = __ffma2_rn(dtp[t], A2[r], f2(kEx2ArgShift, kEx2ArgShift));
-            const float2 dA = f2(ex2(arg.x), ex2(arg.y));
+            const float2 dA = decay(__ffma2_rn(dtp[t], A2[r], f2(kArg, kArg)));
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
             h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
@@ -510,13 +539,17 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
     }
     if (pass == 0 && !timed_out && seg != p.skip_publish) {
       // Publish this segment's aggregate: end state from a zero start, and its summed step.
-      float* my_agg = p.agg + (unit * 32 + lane) * (K + 1);
+      float* my_agg = p.agg + (unit * 32 + lane) * (2 * K);
 #pragma unroll
       for (int r = 0; r < KP; ++r) {
         my_agg[2 * r] = h[r].x;
         my_agg[2 * r + 1] = h[r].y;
+        if constexpr (EULER) {
+          my_agg[K + 2 * r] = Pr[r].x;
+          my_agg[K + 2 * r + 1] = Pr[r].y;
+        }
       }
-      my_agg[K] = sd;
+      if constexpr (!EULER) my_agg[K] = sd;
       __threadfence();
       __syncwarp();
       if (lane == 0) st_release(p.flags + unit, kFlagAgg);
@@ -646,7 +679,7 @@ cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Works
   const size_t bc_bytes = widen ? align128(rows * kNP * sizeof(float)) : 0;
   const size_t flag_bytes = carry_units ? align128(sizeof(unsigned) * (1 + carry_units)) : 0;
   const size_t carry_bytes =
-      carry_units ? flag_bytes + carry_units * 32 * (K + 1) * sizeof(float) : 0;
+      carry_units ? flag_bytes + carry_units * 32 * (2 * K) * sizeof(float) : 0;
   const size_t bytes = 2 * bc_bytes + carry_bytes;
   w->own = a.scratch == nullptr;
   cudaError_t e = cudaSuccess;
@@ -702,6 +735,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   p.A = a.A;
   p.D = a.D;
   p.bias = a.bias;
+  p.h0 = a.h0;
   p.h_last = a.h_last;
   p.status = a.status;
   p.L = int(a.L);
@@ -730,7 +764,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   return p;
 }
 
-template <typename IO, int G>
+template <typename IO, int G, bool EULER>
 cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
   constexpr int CPW = 32 / G;
   constexpr int K = kNP / G;
@@ -764,7 +798,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
             make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
             make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
   if (!ok) return w.release(cudaErrorInvalidValue);
-  auto kern = sscan_lane_kernel<IO, G, kLaneTC>;
+  auto kern = sscan_lane_kernel<IO, G, kLaneTC, EULER>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return w.release(e);
   if (p.n_seg > 1) {
@@ -775,6 +809,13 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
     kern<<<grid, threads, smem_bytes, a.stream>>>(mu, md, mz, mB, mC, my, p);
   }
   return w.release(cudaGetLastError());
+}
+
+template <typename IO, bool EULER>
+cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int segments) {
+  if (G == 1) return launch_lane_typed<IO, 1, EULER>(a, threads, stages, segments);
+  if (G == 2) return launch_lane_typed<IO, 2, EULER>(a, threads, stages, segments);
+  return launch_lane_typed<IO, 4, EULER>(a, threads, stages, segments);
 }
 
 }  // namespace
@@ -796,15 +837,11 @@ cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
   const int st = tune.stages, sg = tune.segments;
-  if (a.io == Io::F32) {
-    if (G == 1) return launch_lane_typed<float, 1>(a, threads, st, sg);
-    if (G == 2) return launch_lane_typed<float, 2>(a, threads, st, sg);
-    return launch_lane_typed<float, 4>(a, threads, st, sg);
-  }
+  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg)
+                                      : launch_lane_g<float, false>(a, G, threads, st, sg);
   using bf = __nv_bfloat16;
-  if (G == 1) return launch_lane_typed<bf, 1>(a, threads, st, sg);
-  if (G == 2) return launch_lane_typed<bf, 2>(a, threads, st, sg);
-  return launch_lane_typed<bf, 4>(a, threads, st, sg);
+  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg)
+                 : launch_lane_g<bf, false>(a, G, threads, st, sg);
 }
 
 TmaTuning tuning_from_env() {
@@ -829,25 +866,90 @@ bool tma_path_ok(const FwdArgs& a) {
 
 cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& tune) { return launch_lane(a, tune); }
 
-cudaError_t launch_simple(const FwdArgs& a) {
+namespace {
+
+template <typename IO, bool EULER>
+cudaError_t launch_simple_typed(const FwdArgs& a) {
   const int64_t chans = a.batch * a.dim;
   const int threads = 128;
   const unsigned blocks = unsigned((chans + threads - 1) / threads);
-  if (a.io == Io::F32) {
-    sscan_simple_kernel<float><<<blocks, threads, 0, a.stream>>>(
-        static_cast<const float*>(a.u), static_cast<const float*>(a.delta), a.A,
-        static_cast<const float*>(a.B), static_cast<const float*>(a.C), a.D,
-        static_cast<const float*>(a.z), a.bias, a.softplus, static_cast<float*>(a.y), a.h_last,
-        a.batch, a.L, a.dim, int(a.N));
-  } else {
-    using bf = __nv_bfloat16;
-    sscan_simple_kernel<bf><<<blocks, threads, 0, a.stream>>>(
-        static_cast<const bf*>(a.u), static_cast<const bf*>(a.delta), a.A,
-        static_cast<const bf*>(a.B), static_cast<const bf*>(a.C), a.D,
-        static_cast<const bf*>(a.z), a.bias, a.softplus, static_cast<bf*>(a.y), a.h_last,
-        a.batch, a.L, a.dim, int(a.N));
-  }
+  sscan_simple_kernel<IO, EULER><<<blocks, threads, 0, a.stream>>>(
+      static_cast<const IO*>(a.u), static_cast<const IO*>(a.delta), a.A,
+      static_cast<const IO*>(a.B), static_cast<const IO*>(a.C), a.D,
+      static_cast<const IO*>(a.z), a.bias, a.softplus, a.h0, static_cast<IO*>(a.y), a.h_last,
+      a.batch, a.L, a.dim, int(a.N));
   return cudaGetLastError();
+}
+
+// One step of the recurrence (recurrent / decode mode): four lanes per (batch, channel), lane q
+// holding states 4q .. 4q + 3 of the state h (batch, dim, N), which is read and written in place.
+// u, delta, z, y are (batch, dim); B, C (batch, N). The per-channel work (softplus, skip, gate)
+// is repeated by the four lanes; the readout is summed with two shuffles.
+template <typename IO, bool EULER>
+__global__ void __launch_bounds__(256) sscan_step_kernel(
+    const IO* __restrict__ u, const IO* __restrict__ delta, const float* __restrict__ A,
+    const IO* __restrict__ Bm, const IO* __restrict__ Cm, const float* __restrict__ Dskip,
+    const IO* __restrict__ z, const float* __restrict__ bias, int softplus, float* __restrict__ h,
+    IO* __restrict__ y, int64_t batch, int64_t dim, int N) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t c = gid >> 2;  // channel b * dim + d
+  const int q = int(threadIdx.x & 3);
+  const bool live = c < batch * dim;
+  const int64_t b = live ? c / dim : 0, d = live ? c - b * dim : 0;
+  float part = 0.f, uu = 0.f;
+  if (live) {
+    const float x = to_f32(delta[c]) + (bias ? bias[d] : 0.f);
+    const float dt = softplus ? softplus_f(x) : x;
+    uu = to_f32(u[c]);
+    const float dtu = dt * uu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * q + i;
+      if (n < N) {
+        const float e = EULER ? fmaf(dt, A[d * N + n], 1.f)
+                              : ex2(fmaf(dt, A[d * N + n] * kLog2e, kEx2ArgShift));
+        const float hn = fmaf(e, h[c * N + n], dtu * to_f32(Bm[b * N + n]));
+        h[c * N + n] = hn;
+        part = fmaf(to_f32(Cm[b * N + n]), hn, part);
+      }
+    }
+  }
+  part += __shfl_xor_sync(0xffffffffu, part, 1);
+  part += __shfl_xor_sync(0xffffffffu, part, 2);
+  if (live && q == 0) {
+    float yv = Dskip ? fmaf(Dskip[d], uu, part) : part;
+    if (z) yv *= silu_f(to_f32(z[c]));
+    store_io(y + c, yv);
+  }
+}
+
+template <typename IO, bool EULER>
+cudaError_t launch_step_typed(const FwdArgs& a) {
+  const int64_t lanes = a.batch * a.dim * 4;
+  const int threads = 256;
+  const unsigned blocks = unsigned((lanes + threads - 1) / threads);
+  sscan_step_kernel<IO, EULER><<<blocks, threads, 0, a.stream>>>(
+      static_cast<const IO*>(a.u), static_cast<const IO*>(a.delta), a.A,
+      static_cast<const IO*>(a.B), static_cast<const IO*>(a.C), a.D,
+      static_cast<const IO*>(a.z), a.bias, a.softplus, a.h_last, static_cast<IO*>(a.y), a.batch,
+      a.dim, int(a.N));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simple(const FwdArgs& a) {
+  if (a.io == Io::F32)
+    return a.euler ? launch_simple_typed<float, true>(a) : launch_simple_typed<float, false>(a);
+  using bf = __nv_bfloat16;
+  return a.euler ? launch_simple_typed<bf, true>(a) : launch_simple_typed<bf, false>(a);
+}
+
+cudaError_t launch_step(const FwdArgs& a) {
+  if (a.io == Io::F32)
+    return a.euler ? launch_step_typed<float, true>(a) : launch_step_typed<float, false>(a);
+  using bf = __nv_bfloat16;
+  return a.euler ? launch_step_typed<bf, true>(a) : launch_step_typed<bf, false>(a);
 }
 
 }  // namespace sscan

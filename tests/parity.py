@@ -61,13 +61,14 @@ def io_name(t: torch.Tensor) -> str:
     return "f32" if t.dtype == torch.float32 else "bf16"
 
 
-def oracle_full(x: dict, softplus: bool = True):
-    """Oracle on whole tensors (small workloads)."""
+def oracle_full(x: dict, softplus: bool = True, h0=None, euler: bool = False):
+    """Oracle on whole tensors (small workloads); h0 a float32 torch tensor or None."""
     io = io_name(x["u"])
     g = lambda k: None if x.get(k) is None else to_np_io(x[k])  # noqa: E731
     f = lambda k: None if x.get(k) is None else x[k].detach().cpu().numpy()  # noqa: E731
     return oracle.fwd(g("u"), g("delta"), f("A"), g("B"), g("C"), f("D"), g("z"),
-                      f("delta_bias"), softplus=softplus, io=io)
+                      f("delta_bias"), softplus=softplus, io=io,
+                      h0=None if h0 is None else h0.detach().cpu().numpy(), euler=euler)
 
 
 def oracle_channels(x: dict, chans, softplus: bool = True):

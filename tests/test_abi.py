@@ -56,3 +56,17 @@ def test_argument_errors_are_synchronous_without_a_device(lib):
     args = list(ok)
     args[11], args[12], args[13] = 1 << 40, 1 << 40, 64
     assert lib.sscan_fwd(*args) == 1
+    # sscan_fwd_ex: the same checks, plus an out-of-range decay-factor selector
+    ok_ex = ok[:9] + [None, 0] + ok[9:]
+    for idx, val in [(16, 0), (16, 17), (14, -1), (2, None), (11, None), (10, 2), (10, -1)]:
+        args = list(ok_ex)
+        args[idx] = val
+        assert lib.sscan_fwd_ex(*args) == 1, (idx, val)
+    # sscan_step: u, delta, A, B, C, D, z, bias, softplus, disc, h, y, batch, dim, N, dtype, stream
+    ok_st = [dummy, dummy, dummy, dummy, dummy, None, None, None, 1, 0, dummy, dummy, 4, 64, 16,
+             0, None]
+    for idx, val in [(14, 0), (14, 17), (12, -1), (13, -1), (15, 2), (9, 5), (10, None),
+                     (11, None), (0, None), (2, None)]:
+        args = list(ok_st)
+        args[idx] = val
+        assert lib.sscan_step(*args) == 1, (idx, val)
