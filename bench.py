@@ -12,6 +12,11 @@ slowest rank's time is used: value = N * units / max_time ("scaling": "weak").
 
 --impl reference times the fp64 CPU oracle (the correctness reference) on a bounded sample of
 the same workload per step, on this machine's host cores.
+
+--mode decode times the single-step recurrence (sscan_step) on the workload's batch, channels
+and state size instead: one step per token, the state read and written in place, as K
+back-to-back launches and as CUDA-graph replays of 64 captured steps; the roofline is HBM on the
+state plus the step's inputs and outputs.
 """
 from __future__ import annotations
 
@@ -46,6 +51,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mode", choices=["scan", "decode"], default="scan")
     return ap.parse_args()
 
 
@@ -300,6 +306,84 @@ def config_of(w):
             "l2": f"inputs larger than L2 ({w.io_bytes() / 1e6:.0f} MB footprint vs 126 MiB L2)"}
 
 
+def run_decode(args, w):
+    """Single-step decode (sscan_step) on the workload's (batch, dim, N): JSON line on stdout."""
+    import torch
+
+    from selective_state_space_158_b300 import binding
+    from selective_state_space_158_b300.inputs import make_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load()
+    # Enough concurrent sequences that the state (read and written every step) is twice the
+    # 126 MiB L2: the step then streams the state from HBM instead of finding it in L2.
+    batch = max(w.batch, math.ceil(2 * L2_BYTES / (w.dim * w.N * 4)))
+    w = w.replace(L=1, batch=batch)
+    x = make_inputs(w, device=dev)
+    one = {k: (v[:, 0].contiguous() if v is not None and v.dim() == 3 else v)
+           for k, v in x.items()}
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    h = torch.randn((w.batch, w.dim, w.N), generator=g, device=dev, dtype=torch.float32) * 0.1
+    y = torch.empty_like(one["u"])
+
+    def step(stream=None):
+        binding.step(one["u"], one["delta"], one["A"], one["B"], one["C"], h, D=one.get("D"),
+                     z=one.get("z"), delta_bias=one.get("delta_bias"), y=y, stream=stream)
+
+    stream = torch.cuda.Stream(dev)
+    K = max(64, args.steps - args.steps % 64)
+    for _ in range(max(3, args.warmup)):
+        step(stream)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as cs:
+        ev0.record(stream)
+        for _ in range(K):
+            step(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms_launch = ev0.elapsed_time(ev1) / K
+    # 64 steps captured once, replayed K / 64 times
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(64):
+            step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev0.record()
+    for _ in range(K // 64):
+        graph.replay()
+    ev1.record()
+    torch.cuda.synchronize(dev)
+    ms_graph = ev0.elapsed_time(ev1) / K
+    es = 4 if w.io == "f32" else 2
+    bdn = w.batch * w.dim * w.N
+    bytes_ = (2 * bdn * 4 + w.dim * w.N * 4 + w.dim * 4 * (int(w.has_D) + int(w.has_bias))
+              + w.batch * w.dim * es * (3 + int(w.has_z)) + 2 * w.batch * w.N * es)
+    hbm_gbs, _, peak_src = peaks()
+    gbs = bytes_ / (ms_graph / 1e3) / 1e9
+    line = {
+        "metric": "selective-scan decode step (sscan_step): (B·D·N)/s and GB/s on 1 B300",
+        "value": bdn / (ms_graph / 1e3), "unit": "(B*D*N)/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_graph, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.io, "data": "synthetic (seeded)",
+        "config": {"workload": f"decode step, batch {w.batch}, D {w.dim}, N {w.N}, {w.io}",
+                   "batch": w.batch, "D": w.dim, "N": w.N, "z_gate": w.has_z,
+                   "D_skip": w.has_D, "timing": "CUDA graph of 64 steps, replayed",
+                   "l2": f"state {bdn * 4 / 1e6:.0f} MB, twice the 126 MiB L2"},
+        "gpu_launches": K,
+        "launch_ms_per_step": ms_launch,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": gbs / hbm_gbs, "traffic": None, "bytes_per_step": bytes_,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "clocks": cs.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from selective_state_space_158_b300.inputs import WORKLOADS
@@ -307,6 +391,9 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.mode == "decode":
+        run_decode(args, w)
         return
 
     import torch

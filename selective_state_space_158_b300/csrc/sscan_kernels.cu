@@ -881,11 +881,22 @@ cudaError_t launch_simple_typed(const FwdArgs& a) {
   return cudaGetLastError();
 }
 
+// Four consecutive io values as floats (16-byte load for fp32, 8-byte for bf16).
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+  const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+  return make_float4(a.x, a.y, c.x, c.y);
+}
+
 // One step of the recurrence (recurrent / decode mode): four lanes per (batch, channel), lane q
 // holding states 4q .. 4q + 3 of the state h (batch, dim, N), which is read and written in place.
 // u, delta, z, y are (batch, dim); B, C (batch, N). The per-channel work (softplus, skip, gate)
-// is repeated by the four lanes; the readout is summed with two shuffles.
-template <typename IO, bool EULER>
+// is repeated by the four lanes; the readout is summed with two shuffles. VEC: N a multiple of 4
+// and rows aligned, so a lane moves its states, A, B and C with one vector access each (the
+// state is streamed through with evict-first hints: it is read and written once per step).
+template <typename IO, bool EULER, bool VEC>
 __global__ void __launch_bounds__(256) sscan_step_kernel(
     const IO* __restrict__ u, const IO* __restrict__ delta, const float* __restrict__ A,
     const IO* __restrict__ Bm, const IO* __restrict__ Cm, const float* __restrict__ Dskip,
@@ -897,7 +908,26 @@ __global__ void __launch_bounds__(256) sscan_step_kernel(
   const bool live = c < batch * dim;
   const int64_t b = live ? c / dim : 0, d = live ? c - b * dim : 0;
   float part = 0.f, uu = 0.f;
-  if (live) {
+  if (live && VEC && 4 * q < N) {
+    const float x = to_f32(delta[c]) + (bias ? bias[d] : 0.f);
+    const float dt = softplus ? softplus_f(x) : x;
+    uu = to_f32(u[c]);
+    const float dtu = dt * uu;
+    float4* hp = reinterpret_cast<float4*>(h + c * N + 4 * q);
+    const float4 hv = __ldcs(hp);
+    const float4 av = load4(A + d * N + 4 * q);
+    const float4 bv = load4(Bm + b * N + 4 * q), cv = load4(Cm + b * N + 4 * q);
+    auto fac = [&](float a) {
+      return EULER ? fmaf(dt, a, 1.f) : ex2(fmaf(dt, a * kLog2e, kEx2ArgShift));
+    };
+    float4 hn;
+    hn.x = fmaf(fac(av.x), hv.x, dtu * bv.x);
+    hn.y = fmaf(fac(av.y), hv.y, dtu * bv.y);
+    hn.z = fmaf(fac(av.z), hv.z, dtu * bv.z);
+    hn.w = fmaf(fac(av.w), hv.w, dtu * bv.w);
+    __stcs(hp, hn);
+    part = fmaf(cv.x, hn.x, fmaf(cv.y, hn.y, fmaf(cv.z, hn.z, cv.w * hn.w)));
+  } else if (live && !VEC) {
     const float x = to_f32(delta[c]) + (bias ? bias[d] : 0.f);
     const float dt = softplus ? softplus_f(x) : x;
     uu = to_f32(u[c]);
@@ -928,7 +958,11 @@ cudaError_t launch_step_typed(const FwdArgs& a) {
   const int64_t lanes = a.batch * a.dim * 4;
   const int threads = 256;
   const unsigned blocks = unsigned((lanes + threads - 1) / threads);
-  sscan_step_kernel<IO, EULER><<<blocks, threads, 0, a.stream>>>(
+  auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; };
+  const bool vec = a.N % 4 == 0 && al(a.h_last, 16) && al(a.A, 16) &&
+                   al(a.B, 4 * sizeof(IO)) && al(a.C, 4 * sizeof(IO));
+  auto kern = vec ? sscan_step_kernel<IO, EULER, true> : sscan_step_kernel<IO, EULER, false>;
+  kern<<<blocks, threads, 0, a.stream>>>(
       static_cast<const IO*>(a.u), static_cast<const IO*>(a.delta), a.A,
       static_cast<const IO*>(a.B), static_cast<const IO*>(a.C), a.D,
       static_cast<const IO*>(a.z), a.bias, a.softplus, a.h_last, static_cast<IO*>(a.y), a.batch,
