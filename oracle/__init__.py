@@ -65,6 +65,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sscan_oracle_channel_ex.argtypes = [vp, vp, vp, i64, fp, vp, vp, fp, fp, ci, fp, ci,
                                             i64, i64, ci, dp, i64, dp, dp]
     lib.sscan_oracle_channel_ex.restype = None
+    lib.sscan_oracle_conv1d.argtypes = [vp, fp, fp, vp, ci, dp, i64, i64, i64, i64, ci]
+    lib.sscan_oracle_conv1d.restype = ci
     _lib_cache[path] = lib
     return lib
 
@@ -151,3 +153,28 @@ def fwd_channel(u, delta, A_d, B, C, Dskip_d=None, z=None, bias_d=None, softplus
                                 int(bool(euler)), L, N, int(io == "bf16"), _ptr(y), 1, _ptr(h),
                                 _ptr(mag))
     return (y, h, mag) if want_mag else (y, h)
+
+
+def conv1d(x, w, bias=None, x_prev=None, silu: bool = True, io: str = "f32", lib=None):
+    """Causal depthwise convolution over time, then SiLU (see ``sscan_oracle_conv1d``).
+
+    x: (batch, L, dim) io array; w: (dim, width) float32; bias: (dim,) float32 or None; x_prev:
+    (batch, width - 1, dim) io array or None (zeros before t = 0). Returns y (batch, L, dim)
+    float64.
+    """
+    lib = lib or load()
+    x = _io_array(x, io)
+    batch, L, dim = x.shape
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert w.shape[0] == dim
+    width = w.shape[1]
+    bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if x_prev is not None:
+        x_prev = _io_array(x_prev, io)
+        assert x_prev.shape == (batch, width - 1, dim)
+    y = np.empty((batch, L, dim), dtype=np.float64)
+    rc = lib.sscan_oracle_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev), int(bool(silu)),
+                                 _ptr(y), batch, L, dim, width, int(io == "bf16"))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return y

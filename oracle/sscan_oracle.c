@@ -250,3 +250,53 @@ int sscan_oracle_fwd(const void *u, const void *delta, const float *A, const voi
   return sscan_oracle_fwd_ex(u, delta, A, B, C, Dskip, z, delta_bias, softplus_flag, NULL, 0, y,
                              h_last, ymag, batch, L, dim, N, io_bf16, nthreads);
 }
+
+/*
+ * Causal depthwise convolution over time, then SiLU: the step that turns the in-projection's
+ * output into the scan's input in the Mamba block ([notes] "架构：极简设计": Linear -> Conv1d ->
+ * SiLU). Per channel d, with W = width taps and w[d, W-1] the tap of the current step:
+ *
+ *   acc = bias[d] + sum_{j=0}^{W-1} w[d, j] * x[b, t - (W-1) + j, d]
+ *   y[b, t, d] = silu ? acc / (1 + e^-acc) : acc
+ *
+ * Inputs before t = 0 come from x_prev (batch, W-1, dim), oldest first, or are zero. Causal
+ * (no future step enters) and depthwise (channels do not mix): the plainest reading of a
+ * convolution placed ahead of a causal, per-channel recurrence. Width is a parameter (the pages
+ * do not give it). Layouts: x (batch, L, dim) io; w (dim, W) fp32; bias (dim) fp32 or NULL;
+ * y (batch, L, dim) double. Returns 0, or -1 on bad sizes.
+ */
+int sscan_oracle_conv1d(const void *x, const float *w, const float *bias, const void *x_prev,
+                        int silu, double *y, int64_t batch, int64_t L, int64_t dim,
+                        int64_t width, int io_bf16) {
+  if (batch < 0 || L < 0 || dim < 0 || width < 1) return -1;
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t d = 0; d < dim; ++d)
+      for (int64_t t = 0; t < L; ++t) {
+        double acc = bias ? (double)bias[d] : 0.0;
+#if SSCAN_ORACLE_MUTANT == 18
+        acc = 0.0; /* mutant: bias dropped */
+#endif
+        for (int64_t j = 0; j < width; ++j) {
+#if SSCAN_ORACLE_MUTANT == 15
+          int64_t s = t + j; /* mutant: future steps instead of past ones */
+#elif SSCAN_ORACLE_MUTANT == 16
+          int64_t s = t - j; /* mutant: taps applied in reverse order */
+#else
+          int64_t s = t - (width - 1) + j;
+#endif
+          double v = 0.0;
+          if (s >= 0 && s < L)
+            v = widen(x, (b * L + s) * dim + d, io_bf16);
+          else if (s < 0 && x_prev)
+            v = widen(x_prev, (b * (width - 1) + (s + width - 1)) * dim + d, io_bf16);
+          acc += (double)w[d * width + j] * v;
+        }
+#if SSCAN_ORACLE_MUTANT == 17
+        y[(b * L + t) * dim + d] = acc; /* mutant: SiLU dropped */
+        (void)silu;
+#else
+        y[(b * L + t) * dim + d] = silu ? acc / (1.0 + exp(-acc)) : acc;
+#endif
+      }
+  return 0;
+}

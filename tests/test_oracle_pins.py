@@ -434,9 +434,48 @@ def pin_euler_lti(lib=None):
             np.testing.assert_allclose(y[b, :, d], ref, rtol=1e-11, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------------------------
+# 11. Causal depthwise Conv1d + SiLU ahead of the scan ("Mamba: Linear-Time Sequence Modeling
+#     with Selective State Spaces" notes, "架构：极简设计": Linear -> Conv1d -> SiLU).
+# ---------------------------------------------------------------------------------------------
+def pin_conv1d_numpy(lib=None):
+    """Against numpy.convolve with the taps reversed (w[W-1] weighs the current step) and
+    scipy's logistic function; widths 1 .. 5."""
+    rng = np.random.default_rng(31)
+    batch, L, dim = 2, 23, 3
+    x = _f32(rng.standard_normal((batch, L, dim)))
+    for width in range(1, 6):
+        w = _f32(rng.standard_normal((dim, width)))
+        bias = _f32(rng.standard_normal(dim))
+        y = oracle.conv1d(x, w, bias, lib=lib)
+        y_lin = oracle.conv1d(x, w, None, silu=False, lib=lib)
+        for b in range(batch):
+            for d in range(dim):
+                lin = np.convolve(x[b, :, d].astype(np.float64),
+                                  w[d, ::-1].astype(np.float64))[:L]
+                np.testing.assert_allclose(y_lin[b, :, d], lin, rtol=1e-13, atol=1e-13)
+                a = lin + float(bias[d])
+                np.testing.assert_allclose(y[b, :, d], a * expit(a), rtol=1e-12, atol=1e-13)
+
+
+def pin_conv1d_stream(lib=None):
+    """With the previous W - 1 inputs given, the output is the tail of one convolution over the
+    concatenated sequence (a streamed sequence matches an unsplit one)."""
+    rng = np.random.default_rng(32)
+    batch, L, dim, width = 2, 19, 4, 4
+    x = _f32(rng.standard_normal((batch, L + width - 1, dim)))
+    w = _f32(rng.standard_normal((dim, width)))
+    bias = _f32(rng.standard_normal(dim))
+    full = oracle.conv1d(x, w, bias, lib=lib)
+    tail = oracle.conv1d(x[:, width - 1:].copy(), w, bias, x_prev=x[:, :width - 1].copy(),
+                         lib=lib)
+    np.testing.assert_array_equal(tail, full[:, width - 1:])
+
+
 PINS = [pin_worked_example, pin_selective_demo, pin_lti_convolution, pin_matrix_form,
         pin_associativity, pin_delta_zero, pin_skip_gate, pin_softplus, pin_bf16_widening,
-        pin_h0_free_decay, pin_h0_superposition, pin_h0_split_sequence, pin_euler_lti]
+        pin_h0_free_decay, pin_h0_superposition, pin_h0_split_sequence, pin_euler_lti,
+        pin_conv1d_numpy, pin_conv1d_stream]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -476,6 +515,10 @@ MUTANTS = {
     12: "initial state ignored",
     13: "initial state not decayed at the first step",
     14: "Euler factor with the page's sign (1 - dt A)",
+    15: "convolution reads future steps",
+    16: "convolution taps in reverse order",
+    17: "SiLU after the convolution dropped",
+    18: "convolution bias dropped",
 }
 
 
