@@ -13,6 +13,10 @@ slowest rank's time is used: value = N * units / max_time ("scaling": "weak").
 --impl reference times the fp64 CPU oracle (the correctness reference) on a bounded sample of
 the same workload per step, on this machine's host cores.
 
+--mode conv times the causal depthwise Conv1d + SiLU (sscan_conv1d_silu) over the workload's
+(batch, L, dim) in its io type; the roofline is HBM on the input read once, the output written
+once and the tiles' halos.
+
 --mode decode times the single-step recurrence (sscan_step) on the workload's batch, channels
 and state size instead: one step per token, the state read and written in place, as K
 back-to-back launches and as CUDA-graph replays of 64 captured steps; the roofline is HBM on the
@@ -51,7 +55,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["scan", "decode"], default="scan")
+    ap.add_argument("--mode", choices=["scan", "decode", "conv"], default="scan")
+    ap.add_argument("--conv-width", type=int, default=4)
     return ap.parse_args()
 
 
@@ -384,6 +389,71 @@ def run_decode(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_conv(args, w):
+    """Conv1d + SiLU over the workload's x: JSON line on stdout."""
+    import torch
+
+    from selective_state_space_158_b300 import binding
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load()
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    dt = torch.float32 if w.io == "f32" else torch.bfloat16
+    W = args.conv_width
+    x = torch.randn((w.batch, w.L, w.dim), generator=g, device=dev).to(dt)
+    wt = torch.randn((w.dim, W), generator=g, device=dev) * 0.5
+    bias = torch.randn((w.dim,), generator=g, device=dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        binding.conv1d_silu(x, wt, bias, y=y, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    # 16 launches captured once and replayed, so that host-side argument checks do not pace the
+    # GPU for this short kernel.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(16):
+            binding.conv1d_silu(x, wt, bias, y=y)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    K = max(16, args.steps - args.steps % 16)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as cs:
+        ev0.record()
+        for _ in range(K // 16):
+            graph.replay()
+        ev1.record()
+        torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / K
+    es = 4 if w.io == "f32" else 2
+    bld = w.batch * w.L * w.dim
+    bytes_ = 2 * bld * es + w.dim * (W + 1) * 4
+    hbm_gbs, _, peak_src = peaks()
+    gbs = bytes_ / (ms / 1e3) / 1e9
+    line = {
+        "metric": "causal depthwise conv1d + SiLU (sscan_conv1d_silu): (B·L·D)/s and GB/s on 1 B300",
+        "value": bld / (ms / 1e3), "unit": "(B*L*D)/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.io, "data": "synthetic (seeded)",
+        "config": {"workload": f"conv1d width {W} + SiLU on {w.name}", "batch": w.batch,
+                   "L": w.L, "D": w.dim, "width": W,
+                   "timing": "CUDA graph of 16 launches, replayed",
+                   "l2": f"input {bld * es / 1e6:.0f} MB vs 126 MiB L2"},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": gbs / hbm_gbs, "traffic": None, "bytes_per_step": bytes_,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "clocks": cs.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from selective_state_space_158_b300.inputs import WORKLOADS
@@ -394,6 +464,9 @@ def main():
         return
     if args.mode == "decode":
         run_decode(args, w)
+        return
+    if args.mode == "conv":
+        run_conv(args, w)
         return
 
     import torch

@@ -118,6 +118,28 @@ sscan_status_t sscan_step(const void* u, const void* delta, const float* A, cons
                           int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * sscan_conv1d_silu -- causal depthwise convolution over time followed by SiLU: the step that
+ * turns the Mamba block's in-projection output into the scan's input u ("Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces" notes, "架构：极简设计": Linear -> Conv1d ->
+ * SiLU). For every batch row b, channel d and step t, with W = width:
+ *
+ *   y[b,t,d] = SiLU(bias[d] + sum_{j=0}^{W-1} w[d,j] * x[b, t-(W-1)+j, d])   (SiLU if silu_flag)
+ *
+ * The pages give neither the width nor the tap order; the convolution is causal (no future
+ * step enters) and depthwise (channels do not mix), and w[d, W-1] weighs the current step.
+ *   x, y   : (batch, L, dim) device memory, element type `dtype`; y must not alias x
+ *   w      : (dim, width) fp32;  bias: (dim) fp32 or NULL
+ *   x_prev : (batch, width-1, dim) `dtype`, the width-1 inputs before t = 0 (oldest first), for
+ *            continuing a streamed sequence; NULL means zeros
+ * 1 <= width <= 64. Asynchronous on `stream`; allocates nothing; argument errors are synchronous
+ * (SSCAN_ERR_INVALID_ARG), launch errors SSCAN_ERR_CUDA.
+ */
+sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bias,
+                                 const void* x_prev, int silu_flag, void* y, int64_t batch,
+                                 int64_t L, int64_t dim, int64_t width, sscan_dtype_t dtype,
+                                 cudaStream_t stream);
+
+/*
  * sscan_fwd_host -- the same operation on HOST buffers: copies the inputs to the current
  * device on `stream`, runs sscan_fwd, copies y and h_last back and synchronizes `stream`.
  * Arguments mean what they mean for sscan_fwd but every pointer is host memory (page-locked

@@ -31,8 +31,11 @@ _FWD_EX_ARGS = _FWD_ARGS[:9] + [_vp, _int] + _FWD_ARGS[9:]
 # stream.
 _STEP_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp, _vp, _i64, _i64, _i64,
               _int, _vp]
+# sscan_conv1d_silu: x, w, bias, x_prev, silu, y, batch, L, dim, width, dtype, stream.
+_CONV_ARGS = [_vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64, _int, _vp]
 SIGNATURES = {
     "sscan_fwd": (_FWD_ARGS, _int),
+    "sscan_conv1d_silu": (_CONV_ARGS, _int),
     "sscan_fwd_ex": (_FWD_EX_ARGS, _int),
     "sscan_step": (_STEP_ARGS, _int),
     "sscan_fwd_host": (_FWD_ARGS, _int),
@@ -214,6 +217,40 @@ def fwd_host(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
                                   _stream_handle(stream, dev))
     _check(code, "sscan_fwd_host")
     return y, h_last
+
+
+def conv1d_silu(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                x_prev: Optional[torch.Tensor] = None, silu: bool = True,
+                y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal depthwise convolution over time + SiLU through ``sscan_conv1d_silu``.
+
+    x: (batch, L, dim) float32 or bfloat16; w: (dim, width) float32; bias: (dim,) float32;
+    x_prev: (batch, width - 1, dim) in x's dtype (inputs before t = 0). Returns y like x.
+    """
+    lib = load()
+    io = _dtype_code(x)
+    batch, L, dim = x.shape
+    width = w.shape[-1]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("libsscan computes on CUDA tensors only")
+    if tuple(w.shape) != (dim, width) or w.dtype != torch.float32 or w.device != dev:
+        raise ValueError(f"w: expected ({dim}, width) float32 on {dev}")
+    if bias is not None and (tuple(bias.shape) != (dim,) or bias.dtype != torch.float32):
+        raise ValueError("bias: expected (dim,) float32")
+    if x_prev is not None and (tuple(x_prev.shape) != (batch, width - 1, dim) or
+                               x_prev.dtype != x.dtype):
+        raise ValueError(f"x_prev: expected {(batch, width - 1, dim)} {x.dtype}")
+    if any(t is not None and not t.is_contiguous() for t in [x, w, bias, x_prev]):
+        raise ValueError("all tensors must be contiguous")
+    if y is None:
+        y = torch.empty_like(x)
+    with torch.cuda.device(dev):
+        code = lib.sscan_conv1d_silu(_ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev),
+                                     int(bool(silu)), _ptr(y), batch, L, dim, width, io,
+                                     _stream_handle(stream, dev))
+    _check(code, "sscan_conv1d_silu")
+    return y
 
 
 def device_error(stream=None, device=None) -> int:

@@ -189,6 +189,35 @@ sscan_status_t sscan_step(const void* u, const void* delta, const float* A, cons
   return sscan::launch_step(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 
+sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bias,
+                                 const void* x_prev, int silu_flag, void* y, int64_t batch,
+                                 int64_t L, int64_t dim, int64_t width, sscan_dtype_t dtype,
+                                 cudaStream_t stream) {
+  if (dtype != SSCAN_F32 && dtype != SSCAN_BF16) return SSCAN_ERR_INVALID_ARG;
+  if (batch < 0 || L < 0 || dim < 0 || width < 1 || width > 64) return SSCAN_ERR_INVALID_ARG;
+  int64_t bl, bld, bytes;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, dim, &bld) || !mul_ok(bld, 4, &bytes) ||
+      !mul_ok(dim, width, &bytes))
+    return SSCAN_ERR_INVALID_ARG;
+  if (bld == 0) return SSCAN_OK;
+  if (!x || !w || !y || x == y) return SSCAN_ERR_INVALID_ARG;
+  if (current_device() < 0) return SSCAN_ERR_CUDA;
+  sscan::ConvArgs a;
+  a.x = x;
+  a.w = w;
+  a.bias = bias;
+  a.x_prev = width > 1 ? x_prev : nullptr;
+  a.silu = silu_flag != 0;
+  a.y = y;
+  a.batch = batch;
+  a.L = L;
+  a.dim = dim;
+  a.width = width;
+  a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
+  a.stream = stream;
+  return sscan::launch_conv(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
 sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
                               const void* C, const float* D, const void* z,
                               const float* delta_bias, int softplus_flag, void* y, float* h_last,

@@ -63,6 +63,20 @@ cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& t);
 // One step of the recurrence for every (batch, channel); h_last is the state, read and written.
 cudaError_t launch_step(const FwdArgs& a);
 
+// Causal depthwise convolution over time + SiLU (sscan_conv1d_silu), arguments validated.
+struct ConvArgs {
+  const void* x;       // (batch, L, dim) io
+  const float* w;      // (dim, width) fp32
+  const float* bias;   // (dim) fp32, nullable
+  const void* x_prev;  // (batch, width - 1, dim) io, nullable
+  int silu;
+  void* y;             // (batch, L, dim) io
+  int64_t batch, L, dim, width;
+  Io io;
+  cudaStream_t stream;
+};
+cudaError_t launch_conv(const ConvArgs& a);
+
 // Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS from the environment (0: unset).
 TmaTuning tuning_from_env();
 

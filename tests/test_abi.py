@@ -70,3 +70,11 @@ def test_argument_errors_are_synchronous_without_a_device(lib):
         args = list(ok_st)
         args[idx] = val
         assert lib.sscan_step(*args) == 1, (idx, val)
+    # sscan_conv1d_silu: x, w, bias, x_prev, silu, y, batch, L, dim, width, dtype, stream
+    other = ctypes.c_void_p(512)
+    ok_cv = [dummy, dummy, None, None, 1, other, 2, 16, 64, 4, 0, None]
+    for idx, val in [(9, 0), (9, 65), (6, -1), (7, -1), (8, -1), (10, 2), (0, None), (1, None),
+                     (5, None), (5, dummy)]:  # the last: y aliasing x
+        args = list(ok_cv)
+        args[idx] = val
+        assert lib.sscan_conv1d_silu(*args) == 1, (idx, val)

@@ -172,3 +172,4 @@ def test_single_decode_step_from_a_given_state():
     yr, hr = oracle_full(x, h0=h_in)
     res = compare(y[:, None, :], h, yr, hr, w.io)
     assert_within(res, w.io, "single step")
+
