@@ -67,6 +67,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sscan_oracle_channel_ex.restype = None
     lib.sscan_oracle_conv1d.argtypes = [vp, fp, fp, vp, ci, dp, i64, i64, i64, i64, ci]
     lib.sscan_oracle_conv1d.restype = ci
+    lib.sscan_oracle_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, ci, vp, fp,
+                                     dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, ci]
+    lib.sscan_oracle_bwd.restype = ci
     _lib_cache[path] = lib
     return lib
 
@@ -178,3 +181,38 @@ def conv1d(x, w, bias=None, x_prev=None, silu: bool = True, io: str = "f32", lib
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     return y
+
+
+def bwd(u, delta, A, B, C, Dskip, z, delta_bias, dy, dh_last=None, softplus: bool = True,
+        h0=None, euler: bool = False, io: str = "f32", lib=None):
+    """Gradients of sum(dy * y) + sum(dh_last * h_last) for the forward of ``fwd`` (see
+    ``sscan_oracle_bwd``). dy: (batch, L, dim) io array; dh_last: (batch, dim, N) float32 or
+    None. Returns a dict of float64 arrays: du, ddelta, dA, dB, dC, and dz / dD / ddelta_bias /
+    dh0 when z / Dskip / delta_bias / h0 are given."""
+    lib = lib or load()
+    u, delta, dy = _io_array(u, io), _io_array(delta, io), _io_array(dy, io)
+    B, C = _io_array(B, io), _io_array(C, io)
+    z = None if z is None else _io_array(z, io)
+    batch, L, dim = u.shape
+    N = B.shape[2]
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    Dskip = None if Dskip is None else np.ascontiguousarray(Dskip, dtype=np.float32)
+    delta_bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    h0 = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float32)
+    dh_last = None if dh_last is None else np.ascontiguousarray(dh_last, dtype=np.float32)
+    out = {"du": np.empty((batch, L, dim)), "ddelta": np.empty((batch, L, dim)),
+           "dA": np.empty((dim, N)), "dB": np.empty((batch, L, N)), "dC": np.empty((batch, L, N))}
+    out["dz"] = np.empty((batch, L, dim)) if z is not None else None
+    out["dD"] = np.empty(dim) if Dskip is not None else None
+    out["ddelta_bias"] = np.empty(dim) if delta_bias is not None else None
+    out["dh0"] = np.empty((batch, dim, N)) if h0 is not None else None
+    rc = lib.sscan_oracle_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                              _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                              int(bool(euler)), _ptr(dy), _ptr(dh_last), _ptr(out["du"]),
+                              _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
+                              _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                              _ptr(out["ddelta_bias"]), _ptr(out["dh0"]), batch, L, dim, N,
+                              int(io == "bf16"))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return {k: v for k, v in out.items() if v is not None}

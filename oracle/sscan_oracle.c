@@ -300,3 +300,127 @@ int sscan_oracle_conv1d(const void *x, const float *w, const float *bias, const 
       }
   return 0;
 }
+
+/*
+ * Backward pass: gradients of  Loss = sum_{b,t,d} dy[b,t,d] * y[b,t,d] + sum dh_last * h_last
+ * with respect to every input of the forward above (the same h0 and factor selector). The
+ * pages fix the method's backward only as "recompute the intermediate states instead of storing
+ * them" ([notes] "第二个创新：硬件感知算法", item 3; [article] 3.3, item 2); the gradient itself
+ * is the derivative of the defined forward, written here as the adjoint recurrence, per channel:
+ *
+ *   forward, keeping every state:  h_t = a_t h_{t-1} + dt_t B_t u_t,  s_t = C_t . h_t + D u_t
+ *   lam_t = dL/dh_t = ds_t C_t + a_{t+1} lam_{t+1},  lam_{L-1} = ds_{L-1} C_{L-1} + dh_last
+ *   ds_t = dy_t g(z_t),  dz_t = dy_t s_t g'(z_t)      (g = SiLU, g' = sig (1 + z (1 - sig)))
+ *   dC_t += ds_t h_t,  dB_t += lam_t dt_t u_t,  du_t = ds_t D + sum_n lam_t dt_t B_t
+ *   d(dt_t) = sum_n lam_t (B_t u_t + h_{t-1} da_t/d(dt)),   da/d(dt) = A a (ZOH) or A (first order)
+ *   dA += lam_t h_{t-1} da_t/dA,                             da/dA = dt a (ZOH) or dt (first order)
+ *   ddelta_t = d(dt_t) sig(x_t) with softplus (1 without),  dbias += ddelta_t,  dD += ds_t u_t
+ *   dh0 = a_0 lam_0
+ *
+ * Outputs (double, overwritten): du, ddelta (batch, L, dim); dz (batch, L, dim) if z; dA
+ * (dim, N); dB, dC (batch, L, N); dD (dim) if Dskip; dbias (dim) if bias; dh0 (batch, dim, N)
+ * if not NULL. dy is (batch, L, dim) io; dh_last (batch, dim, N) fp32 or NULL. Single-threaded
+ * (the parameter gradients sum over channels). Returns 0, or -1 on bad sizes.
+ */
+int sscan_oracle_bwd(const void *u, const void *delta, const float *A, const void *Bm,
+                     const void *Cm, const float *Dskip, const void *z, const float *bias,
+                     int softplus_flag, const float *h0, int euler, const void *dy,
+                     const float *dh_last, double *du, double *ddelta, double *dA, double *dB,
+                     double *dC, double *dD, double *dz, double *dbias, double *dh0,
+                     int64_t batch, int64_t L, int64_t dim, int64_t N, int io_bf16) {
+  if (batch < 0 || L < 0 || dim < 0 || N < 1) return -1;
+  memset(dA, 0, sizeof(double) * (size_t)(dim * N));
+  memset(dB, 0, sizeof(double) * (size_t)(batch * L * N));
+  memset(dC, 0, sizeof(double) * (size_t)(batch * L * N));
+  if (dD) memset(dD, 0, sizeof(double) * (size_t)dim);
+  if (dbias) memset(dbias, 0, sizeof(double) * (size_t)dim);
+  double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N)); /* h_{-1} .. h_{L-1} */
+  double *as = (double *)malloc(sizeof(double) * (size_t)(L * N + 1));
+  double *dts = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+  double *xs = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+  double *ss = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+  double *mu = (double *)malloc(sizeof(double) * (size_t)N);
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t d = 0; d < dim; ++d) {
+      const int64_t cbase = b * L * dim + d; /* element (b, 0, d) */
+      const double Dd = Dskip ? (double)Dskip[d] : 0.0;
+      for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? (double)h0[(b * dim + d) * N + n] : 0.0;
+      for (int64_t t = 0; t < L; ++t) { /* forward, every state kept */
+        const int64_t i = cbase + t * dim;
+        const double x = widen(delta, i, io_bf16) + (bias ? (double)bias[d] : 0.0);
+        const double dt = softplus_flag ? softplus(x) : x;
+        const double ut = widen(u, i, io_bf16);
+        double s = Dd * ut;
+        for (int64_t n = 0; n < N; ++n) {
+          const double a = euler ? 1.0 + dt * (double)A[d * N + n] : exp(dt * (double)A[d * N + n]);
+          const double hn = a * hs[t * N + n] + dt * widen(Bm, (b * L + t) * N + n, io_bf16) * ut;
+          hs[(t + 1) * N + n] = hn;
+          as[t * N + n] = a;
+          s += widen(Cm, (b * L + t) * N + n, io_bf16) * hn;
+        }
+        xs[t] = x;
+        dts[t] = dt;
+        ss[t] = s;
+      }
+      for (int64_t n = 0; n < N; ++n) mu[n] = dh_last ? (double)dh_last[(b * dim + d) * N + n] : 0.0;
+      for (int64_t t = L - 1; t >= 0; --t) { /* adjoint sweep */
+        const int64_t i = cbase + t * dim;
+        const double ut = widen(u, i, io_bf16), dyt = widen(dy, i, io_bf16), dt = dts[t];
+        double ds = dyt;
+        if (z) {
+          const double zt = widen(z, i, io_bf16), sg = 1.0 / (1.0 + exp(-zt));
+          ds = dyt * zt * sg;
+#if SSCAN_ORACLE_MUTANT == 23
+          dz[i] = dyt * ss[t] * sg; /* mutant: gate derivative taken as the sigmoid alone */
+#else
+          dz[i] = dyt * ss[t] * sg * (1.0 + zt * (1.0 - sg));
+#endif
+        }
+        if (dD) dD[d] += ds * ut;
+        double dut = ds * Dd, ddt = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          const double Bt = widen(Bm, (b * L + t) * N + n, io_bf16);
+          const double Ct = widen(Cm, (b * L + t) * N + n, io_bf16);
+          const double An = (double)A[d * N + n], a = as[t * N + n];
+          const double lam = mu[n] + ds * Ct;
+#if SSCAN_ORACLE_MUTANT == 21
+          dC[(b * L + t) * N + n] += ds * hs[t * N + n]; /* mutant: previous state in dC */
+#else
+          dC[(b * L + t) * N + n] += ds * hs[(t + 1) * N + n];
+#endif
+          const double da = lam * hs[t * N + n];
+#if SSCAN_ORACLE_MUTANT == 19
+          (void)An; /* mutant: the decay's dependence on dt dropped */
+#else
+          ddt += euler ? da * An : da * a * An;
+#endif
+          dA[d * N + n] += euler ? da * dt : da * a * dt;
+          ddt += lam * Bt * ut;
+          dB[(b * L + t) * N + n] += lam * dt * ut;
+          dut += lam * dt * Bt;
+#if SSCAN_ORACLE_MUTANT == 20
+          mu[n] = (t > 0 ? as[(t - 1) * N + n] : a) * lam; /* mutant: the earlier step's factor */
+#else
+          mu[n] = a * lam;
+#endif
+        }
+        du[i] = dut;
+#if SSCAN_ORACLE_MUTANT == 22
+        const double dx = ddt; /* mutant: softplus derivative dropped */
+#else
+        const double dx = softplus_flag ? ddt / (1.0 + exp(-xs[t])) : ddt;
+#endif
+        ddelta[i] = dx;
+        if (dbias) dbias[d] += dx;
+      }
+      if (dh0)
+        for (int64_t n = 0; n < N; ++n) dh0[(b * dim + d) * N + n] = mu[n];
+    }
+  free(hs);
+  free(as);
+  free(dts);
+  free(xs);
+  free(ss);
+  free(mu);
+  return 0;
+}

@@ -472,10 +472,114 @@ def pin_conv1d_stream(lib=None):
     np.testing.assert_array_equal(tail, full[:, width - 1:])
 
 
+# ---------------------------------------------------------------------------------------------
+# 12. Backward pass: the gradient of sum(dy * y) + sum(dh_last * h_last). Pinned against torch
+#     autograd of an independent float64 statement of the forward (vectorised over batch,
+#     channels and states) and against central differences of that forward.
+# ---------------------------------------------------------------------------------------------
+def _torch_forward(t, softplus, euler):
+    import torch
+    u, delta, A, Bm, Cm = t["u"], t["delta"], t["A"], t["B"], t["C"]
+    Dv, z, bias, h0 = t.get("D"), t.get("z"), t.get("bias"), t.get("h0")
+    batch, L, dim = u.shape
+    N = A.shape[1]
+    h = h0 if h0 is not None else torch.zeros(batch, dim, N, dtype=torch.float64)
+    ys = []
+    for s in range(L):
+        x = delta[:, s] + (bias if bias is not None else 0.0)
+        dt = torch.nn.functional.softplus(x) if softplus else x
+        a = 1.0 + dt[..., None] * A if euler else torch.exp(dt[..., None] * A)
+        h = a * h + (dt * u[:, s])[..., None] * Bm[:, s, None, :]
+        y = (h * Cm[:, s, None, :]).sum(-1) + (Dv * u[:, s] if Dv is not None else 0.0)
+        if z is not None:
+            y = y * z[:, s] * torch.sigmoid(z[:, s])
+        ys.append(y)
+    return torch.stack(ys, 1), h
+
+
+def _bwd_case(seed, softplus, euler, with_opt):
+    rng = np.random.default_rng(seed)
+    batch, L, dim, N = 2, 13, 3, 4
+    c = {"u": _f32(rng.standard_normal((batch, L, dim))),
+         "delta": _f32(rng.standard_normal((batch, L, dim)) * (0.02 if euler else 1.0)),
+         "A": _f32(-np.exp(rng.uniform(0, math.log(8), (dim, N)))),
+         "B": _f32(rng.standard_normal((batch, L, N))),
+         "C": _f32(rng.standard_normal((batch, L, N)))}
+    if with_opt:
+        c.update({"D": _f32(rng.standard_normal(dim)), "z": _f32(rng.standard_normal((batch, L, dim))),
+                  "bias": _f32(rng.uniform(-3, -1, dim)),
+                  "h0": _f32(rng.standard_normal((batch, dim, N)))})
+    if euler:
+        c["delta"] = _f32(np.abs(c["delta"]))
+    dy = _f32(rng.standard_normal((batch, L, dim)))
+    dh = _f32(rng.standard_normal((batch, dim, N)))
+    return c, dy, dh
+
+
+_BWD_KEYS = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "bias": "ddelta_bias", "h0": "dh0"}
+
+
+def _oracle_grads(c, dy, dh, softplus, euler, lib):
+    return oracle.bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], c.get("D"), c.get("z"),
+                      c.get("bias"), dy, dh, softplus=softplus, h0=c.get("h0"), euler=euler,
+                      lib=lib)
+
+
+def pin_bwd_autograd(lib=None):
+    import torch
+    for seed, softplus, euler, with_opt in [(41, True, False, True), (42, False, True, False),
+                                            (43, True, True, True), (44, False, False, False)]:
+        c, dy, dh = _bwd_case(seed, softplus, euler, with_opt)
+        tt = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in c.items()}
+        y, h = _torch_forward(tt, softplus, euler)
+        # the torch statement computes the same forward as the oracle
+        yo, ho = oracle.fwd(c["u"], c["delta"], c["A"], c["B"], c["C"], c.get("D"), c.get("z"),
+                            c.get("bias"), softplus=softplus, h0=c.get("h0"), euler=euler,
+                            lib=lib)
+        np.testing.assert_allclose(y.detach().numpy(), yo, rtol=1e-12, atol=1e-12)
+        loss = (y * torch.tensor(dy, dtype=torch.float64)).sum() + \
+            (h * torch.tensor(dh, dtype=torch.float64)).sum()
+        loss.backward()
+        g = _oracle_grads(c, dy, dh, softplus, euler, lib)
+        for k, v in tt.items():
+            ref = v.grad.numpy()
+            got = g[_BWD_KEYS[k]]
+            np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-10 * (1 + np.abs(ref).max()),
+                                       err_msg=f"{k} softplus={softplus} euler={euler}")
+
+
+def pin_bwd_finite_difference(lib=None):
+    """Central differences (step 1e-6) of the float64 forward's loss at sampled elements."""
+    import torch
+    softplus, euler = True, False
+    c, dy, dh = _bwd_case(45, softplus, euler, True)
+    g = _oracle_grads(c, dy, dh, softplus, euler, lib)
+    dyt, dht = torch.tensor(dy, dtype=torch.float64), torch.tensor(dh, dtype=torch.float64)
+
+    def loss_of(cc):
+        tt = {k: torch.tensor(v, dtype=torch.float64) for k, v in cc.items()}
+        y, h = _torch_forward(tt, softplus, euler)
+        return float((y * dyt).sum() + (h * dht).sum())
+
+    rng = np.random.default_rng(46)
+    for k, v in c.items():
+        for _ in range(3):
+            idx = tuple(int(rng.integers(0, s)) for s in v.shape)
+            plus = {kk: vv.astype(np.float64) for kk, vv in c.items()}
+            minus = {kk: vv.astype(np.float64) for kk, vv in c.items()}
+            eps = 1e-6
+            plus[k][idx] += eps
+            minus[k][idx] -= eps
+            fd = (loss_of(plus) - loss_of(minus)) / (2 * eps)
+            got = g[_BWD_KEYS[k]][idx]
+            assert abs(got - fd) <= 1e-6 * (1 + abs(fd)), (k, idx, got, fd)
+
+
 PINS = [pin_worked_example, pin_selective_demo, pin_lti_convolution, pin_matrix_form,
         pin_associativity, pin_delta_zero, pin_skip_gate, pin_softplus, pin_bf16_widening,
         pin_h0_free_decay, pin_h0_superposition, pin_h0_split_sequence, pin_euler_lti,
-        pin_conv1d_numpy, pin_conv1d_stream]
+        pin_conv1d_numpy, pin_conv1d_stream, pin_bwd_autograd, pin_bwd_finite_difference]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -519,6 +623,11 @@ MUTANTS = {
     16: "convolution taps in reverse order",
     17: "SiLU after the convolution dropped",
     18: "convolution bias dropped",
+    19: "backward: the decay's dependence on dt dropped",
+    20: "backward: adjoint carried with the earlier step's factor",
+    21: "backward: dC from the previous state",
+    22: "backward: softplus derivative dropped",
+    23: "backward: gate derivative taken as the sigmoid alone",
 }
 
 
