@@ -17,6 +17,10 @@ the same workload per step, on this machine's host cores.
 (batch, L, dim) in its io type; the roofline is HBM on the input read once, the output written
 once and the tiles' halos.
 
+--mode bwd times the backward pass (sscan_bwd: checkpoints, adjoint sweep, reductions) on the
+workload with random dy and dh_last; its compute roofline counts the FP32-pipe operations of a
+recompute plus an adjoint step per update (16) against 128 per clock per SM.
+
 --mode decode times the single-step recurrence (sscan_step) on the workload's batch, channels
 and state size instead: one step per token, the state read and written in place, as K
 back-to-back launches and as CUDA-graph replays of 64 captured steps; the roofline is HBM on the
@@ -55,7 +59,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["scan", "decode", "conv"], default="scan")
+    ap.add_argument("--mode", choices=["scan", "decode", "conv", "bwd"], default="scan")
     ap.add_argument("--conv-width", type=int, default=4)
     return ap.parse_args()
 
@@ -454,6 +458,64 @@ def run_conv(args, w):
     print(json.dumps(line), flush=True)
 
 
+BWD_FP32_OPS_PER_UPDATE = 16  # recompute (4) + adjoint (12) FP32-pipe operations per update
+
+
+def run_bwd(args, w):
+    """Backward pass over the workload: JSON line on stdout."""
+    import torch
+
+    from selective_state_space_158_b300 import binding
+    from selective_state_space_158_b300.inputs import make_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load()
+    x = make_inputs(w, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    dy = torch.randn(x["u"].shape, generator=g, device=dev).to(x["u"].dtype)
+    dh = torch.randn((w.batch, w.dim, w.N), generator=g, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        return binding.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x.get("D"),
+                           z=x.get("z"), delta_bias=x.get("delta_bias"), dh_last=dh,
+                           stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as cs:
+        ev0.record(stream)
+        for _ in range(K):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / K
+    props = torch.cuda.get_device_properties(dev)
+    _, sm_max_mhz, _ = peaks()
+    fp32_peak = props.multi_processor_count * 128 * sm_max_mhz * 1e6  # lane-ops per second
+    ach = w.elems * BWD_FP32_OPS_PER_UPDATE / (ms / 1e3)
+    line = {
+        "metric": "selective-scan backward (sscan_bwd): (B·L·D·N)/s on 1 B300",
+        "value": w.elems / (ms / 1e3), "unit": "(B*L*D*N)/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.io, "data": "synthetic (seeded)",
+        "config": dict(config_of(w), workload=f"backward of {w.name}"),
+        "gpu_launches": 3 * K + (K if (w.io != "f32" or w.N != 16) else 0),
+        "roofline": {"bound": "alu", "achieved": ach / 1e9, "peak": fp32_peak / 1e9,
+                     "unit": "G FP32 lane-ops/s", "frac": ach / fp32_peak, "traffic": None,
+                     "ops_per_update": BWD_FP32_OPS_PER_UPDATE,
+                     "peak_source": f"{props.multi_processor_count} SMs x 128 lanes x "
+                                    f"{sm_max_mhz:.0f} MHz"},
+        "clocks": cs.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from selective_state_space_158_b300.inputs import WORKLOADS
@@ -467,6 +529,9 @@ def main():
         return
     if args.mode == "conv":
         run_conv(args, w)
+        return
+    if args.mode == "bwd":
+        run_bwd(args, w)
         return
 
     import torch

@@ -118,6 +118,37 @@ sscan_status_t sscan_step(const void* u, const void* delta, const float* A, cons
                           int64_t dim, int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * sscan_bwd -- backward pass of sscan_fwd_ex with recomputation: gradients of
+ *     Loss = sum dy * y + sum dh_last * h_last
+ * with respect to every input. The intermediate states are recomputed, not stored ("Mamba:
+ * Linear-Time Sequence Modeling with Selective State Spaces" notes, "第二个创新：硬件感知算法",
+ * item 3; "从RNN到Mamba" 3.3, item 2); the gradient is the adjoint recurrence of the defined
+ * forward.
+ *
+ * Forward inputs (u .. disc) exactly as passed to sscan_fwd_ex. Then:
+ *   dy          : (batch, L, dim) `dtype`, gradient of the loss with respect to y
+ *   dh_last     : (batch, dim, N) fp32 gradient with respect to h_last, or NULL for zero
+ * Outputs (device memory, overwritten):
+ *   du, ddelta  : (batch, L, dim) `dtype`
+ *   dA          : (dim, N) fp32          dB, dC: (batch, L, N) fp32
+ *   dD          : (dim) fp32, required when D is given (else ignored)
+ *   dz          : (batch, L, dim) `dtype`, required when z is given (else ignored)
+ *   ddelta_bias : (dim) fp32, required when delta_bias is given (else ignored)
+ *   dh0         : (batch, dim, N) fp32 gradient with respect to the initial state, or NULL
+ * Parameter gradients (dA, dB, dC, dD, ddelta_bias) are sums over the other axes, reduced in a
+ * fixed order: results are deterministic. Workspace: stream-ordered (cudaMallocAsync) state
+ * checkpoints every 16 steps (batch * dim * N floats each) and per-channel-group partial sums
+ * of dB, dC. Argument errors are synchronous (SSCAN_ERR_INVALID_ARG).
+ */
+sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus_flag, const float* h0, sscan_disc_t disc, const void* dy,
+                         const float* dh_last, void* du, void* ddelta, float* dA, float* dB,
+                         float* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                         int64_t batch, int64_t L, int64_t dim, int64_t N, sscan_dtype_t dtype,
+                         cudaStream_t stream);
+
+/*
  * sscan_conv1d_silu -- causal depthwise convolution over time followed by SiLU: the step that
  * turns the Mamba block's in-projection output into the scan's input u ("Mamba: Linear-Time
  * Sequence Modeling with Selective State Spaces" notes, "架构：极简设计": Linear -> Conv1d ->

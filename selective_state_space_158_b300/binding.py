@@ -33,8 +33,13 @@ _STEP_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp, _vp, _i64
               _int, _vp]
 # sscan_conv1d_silu: x, w, bias, x_prev, silu, y, batch, L, dim, width, dtype, stream.
 _CONV_ARGS = [_vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64, _int, _vp]
+# sscan_bwd: the sscan_fwd_ex inputs (u .. disc), dy, dh_last, du, ddelta, dA, dB, dC, dD, dz,
+# ddelta_bias, dh0, batch, L, dim, N, dtype, stream.
+_BWD_ARGS = [_vp] * 9 + [_vp, _int] + [_vp] * 11 + [_i64] * 4 + [_int, _vp]
+_BWD_ARGS[8] = _int  # softplus_flag
 SIGNATURES = {
     "sscan_fwd": (_FWD_ARGS, _int),
+    "sscan_bwd": (_BWD_ARGS, _int),
     "sscan_conv1d_silu": (_CONV_ARGS, _int),
     "sscan_fwd_ex": (_FWD_EX_ARGS, _int),
     "sscan_step": (_STEP_ARGS, _int),
@@ -217,6 +222,54 @@ def fwd_host(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
                                   _stream_handle(stream, dev))
     _check(code, "sscan_fwd_host")
     return y, h_last
+
+
+def bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+        C: torch.Tensor, dy: torch.Tensor, D: Optional[torch.Tensor] = None,
+        z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+        dh_last: Optional[torch.Tensor] = None, softplus: bool = True,
+        h0: Optional[torch.Tensor] = None, euler: bool = False, want_dh0: bool = False,
+        stream=None) -> dict:
+    """Gradients of sum(dy * y) + sum(dh_last * h_last) through ``sscan_bwd``.
+
+    Forward inputs as for ``fwd``; dy like u; dh_last (batch, dim, N) float32 or None.
+    Returns a dict: du, ddelta (io dtype), dA, dB, dC (float32), and dD / dz / ddelta_bias when
+    D / z / delta_bias are given, dh0 when ``want_dh0``.
+    """
+    lib = load()
+    io = _dtype_code(u)
+    batch, L, dim = u.shape
+    N = B.shape[-1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("libsscan computes on CUDA tensors only")
+    if tuple(dy.shape) != (batch, L, dim) or dy.dtype != u.dtype:
+        raise ValueError("dy must match u")
+    ts = [u, delta, A, B, C, D, z, delta_bias, h0, dy, dh_last]
+    if any(t is not None and (not t.is_contiguous() or t.device != dev) for t in ts):
+        raise ValueError("all tensors must be contiguous and on u's device")
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, L, N), **f32),
+         "dC": torch.empty((batch, L, N), **f32)}
+    if D is not None:
+        g["dD"] = torch.empty((dim,), **f32)
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty((dim,), **f32)
+    if want_dh0:
+        g["dh0"] = torch.empty((batch, dim, N), **f32)
+    with torch.cuda.device(dev):
+        code = lib.sscan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                             _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                             SSCAN_DISC_EULER if euler else SSCAN_DISC_ZOH, _ptr(dy),
+                             _ptr(dh_last), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]),
+                             _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")), _ptr(g.get("dz")),
+                             _ptr(g.get("ddelta_bias")), _ptr(g.get("dh0")), batch, L, dim, N,
+                             io, _stream_handle(stream, dev))
+    _check(code, "sscan_bwd")
+    return g
 
 
 def conv1d_silu(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,

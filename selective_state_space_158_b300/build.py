@@ -9,7 +9,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsscan.so")
-SOURCES = ["sscan_api.cu", "sscan_kernels.cu", "sscan_noalloc.cu", "sscan_conv.cu"]
+SOURCES = ["sscan_api.cu", "sscan_kernels.cu", "sscan_noalloc.cu", "sscan_conv.cu",
+           "sscan_bwd.cu"]
 HEADERS = ["sscan_device.cuh", "sscan_internal.h"]
 
 NVCC_FLAGS = [

@@ -189,6 +189,68 @@ sscan_status_t sscan_step(const void* u, const void* delta, const float* A, cons
   return sscan::launch_step(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 
+sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus_flag, const float* h0, sscan_disc_t disc, const void* dy,
+                         const float* dh_last, void* du, void* ddelta, float* dA, float* dB,
+                         float* dC, float* dD, void* dz, float* ddelta_bias, float* dh0,
+                         int64_t batch, int64_t L, int64_t dim, int64_t N, sscan_dtype_t dtype,
+                         cudaStream_t stream) {
+  if (disc != SSCAN_DISC_ZOH && disc != SSCAN_DISC_EULER) return SSCAN_ERR_INVALID_ARG;
+  int64_t bld = 0, bln = 0;
+  sscan_status_t st = check_args(u, delta, A, B, C, dy, batch, L, dim, N, dtype, &bld, &bln);
+  if (st != SSCAN_OK) return st;
+  if (batch * dim > 0 && L > 0 &&
+      (!du || !ddelta || !dA || !dB || !dC || (D && !dD) || (z && !dz) ||
+       (delta_bias && !ddelta_bias)))
+    return SSCAN_ERR_INVALID_ARG;
+  if (current_device() < 0) return SSCAN_ERR_CUDA;
+  if (batch == 0 || dim == 0) return SSCAN_OK;
+  if (L == 0) {  // nothing depends on the sequence: parameter gradients are zero, dh0 = dh_last
+    cudaError_t e = cudaSuccess;
+    if (dA) e = cudaMemsetAsync(dA, 0, size_t(dim * N) * sizeof(float), stream);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, size_t(dim) * sizeof(float), stream);
+    if (e == cudaSuccess && ddelta_bias)
+      e = cudaMemsetAsync(ddelta_bias, 0, size_t(dim) * sizeof(float), stream);
+    if (e == cudaSuccess && dh0) {
+      const size_t hb = size_t(batch * dim * N) * sizeof(float);
+      e = dh_last ? cudaMemcpyAsync(dh0, dh_last, hb, cudaMemcpyDeviceToDevice, stream)
+                  : cudaMemsetAsync(dh0, 0, hb, stream);
+    }
+    return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+  }
+  sscan::BwdArgs a;
+  a.u = u;
+  a.delta = delta;
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.D = D;
+  a.z = z;
+  a.bias = delta_bias;
+  a.softplus = softplus_flag != 0;
+  a.h0 = h0;
+  a.euler = disc == SSCAN_DISC_EULER;
+  a.dy = dy;
+  a.dh_last = dh_last;
+  a.du = du;
+  a.ddelta = ddelta;
+  a.dA = dA;
+  a.dB = dB;
+  a.dC = dC;
+  a.dD = D ? dD : nullptr;
+  a.dz = z ? dz : nullptr;
+  a.dbias = delta_bias ? ddelta_bias : nullptr;
+  a.dh0 = dh0;
+  a.batch = batch;
+  a.L = L;
+  a.dim = dim;
+  a.N = N;
+  a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
+  a.stream = stream;
+  return sscan::launch_bwd(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
 sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bias,
                                  const void* x_prev, int silu_flag, void* y, int64_t batch,
                                  int64_t L, int64_t dim, int64_t width, sscan_dtype_t dtype,

@@ -77,6 +77,36 @@ struct ConvArgs {
 };
 cudaError_t launch_conv(const ConvArgs& a);
 
+// Backward pass (sscan_bwd), arguments validated.
+struct BwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;       // nullable
+  const void* z;        // nullable
+  const float* bias;    // nullable
+  int softplus;
+  const float* h0;      // nullable
+  int euler;
+  const void* dy;       // (batch, L, dim) io
+  const float* dh_last; // nullable
+  void* du;             // (batch, L, dim) io
+  void* ddelta;         // (batch, L, dim) io
+  float* dA;            // (dim, N)
+  float* dB;            // (batch, L, N)
+  float* dC;            // (batch, L, N)
+  float* dD;            // (dim), required when D is given
+  void* dz;             // (batch, L, dim) io, required when z is given
+  float* dbias;         // (dim), required when bias is given
+  float* dh0;           // (batch, dim, N), nullable
+  int64_t batch, L, dim, N;
+  Io io;
+  cudaStream_t stream;
+};
+cudaError_t launch_bwd(const BwdArgs& a);
+
 // Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS from the environment (0: unset).
 TmaTuning tuning_from_env();
 

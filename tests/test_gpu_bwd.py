@@ -1,0 +1,94 @@
+"""GPU parity of the backward pass (sscan_bwd) against the fp64 adjoint oracle: every gradient,
+both decay factors, optional operands on and off, ragged sizes, bf16 and fp32 io.
+
+Tolerance (the contract states none for gradients): the adjoint recurrence compounds rounding
+like the forward does (same factors, same state memory), and the parameter gradients add up to
+B*L (dA) or D (dB, dC) fp32 terms in a fixed order, whose rounding stays well below the
+recurrence's; so gradients take the forward's bounds and metric: fp32 max 1e-4, and bf16-typed
+gradients (du, ddelta, dz) compared after rounding the oracle to bf16, max 2e-2 and mean 1e-3.
+fp32-typed gradients of bf16 runs take the fp32 bound.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import err_stats, round_bf16, to_np_io
+from selective_state_space_158_b300 import binding
+from selective_state_space_158_b300.inputs import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+TOL_BWD = {"f32": {"max": 1e-4}, "bf16": {"max": 2e-2, "mean": 1e-3}}
+IO_GRADS = ("du", "ddelta", "dz")
+
+
+def _case(io, batch, L, dim, N, euler, opt, seed=3):
+    base = WORKLOADS["fp32"] if io == "f32" else WORKLOADS["bf16"]
+    w = base.replace(batch=batch, L=L, dim=dim, N=N, has_z=opt, has_D=opt, has_bias=opt)
+    x = make_inputs(w, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    dt = x["u"].dtype
+    dy = torch.randn(x["u"].shape, generator=g, device=DEV).to(dt)
+    dh = torch.randn((batch, dim, N), generator=g, device=DEV)
+    h0 = torch.randn((batch, dim, N), generator=g, device=DEV) if opt else None
+    softplus = not euler
+    if euler:  # keep dt |A| < 2 (see the forward tests)
+        x["delta"] = (x["delta"].float().abs() * 0.02).to(dt)
+        x["delta_bias"] = None
+    return w, x, dy, dh, h0, softplus
+
+
+def _check(io, batch, L, dim, N, euler, opt, what):
+    w, x, dy, dh, h0, softplus = _case(io, batch, L, dim, N, euler, opt)
+    got = binding.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x.get("D"), z=x.get("z"),
+                      delta_bias=x.get("delta_bias"), dh_last=dh, softplus=softplus, h0=h0,
+                      euler=euler, want_dh0=True)
+    torch.cuda.synchronize()
+    f = lambda t: None if t is None else t.detach().cpu().numpy()  # noqa: E731
+    ref = oracle.bwd(to_np_io(x["u"]), to_np_io(x["delta"]), f(x["A"]), to_np_io(x["B"]),
+                     to_np_io(x["C"]), f(x.get("D")),
+                     None if x.get("z") is None else to_np_io(x["z"]), f(x.get("delta_bias")),
+                     to_np_io(dy), f(dh), softplus=softplus, h0=f(h0), euler=euler, io=w.io)
+    ref["dh0"] = ref.get("dh0")
+    report = {}
+    for k, r in ref.items():
+        if r is None:
+            continue
+        y = got[k].detach().float().cpu().numpy().astype(np.float64)
+        rr = round_bf16(r) if (w.io == "bf16" and k in IO_GRADS) else r
+        st = err_stats(y, rr)
+        report[k] = st
+        tol = TOL_BWD[w.io] if k in IO_GRADS else TOL_BWD["f32"]
+        assert st["max"] <= tol["max"], f"{what} {k}: max {st['max']:.3g} > {tol['max']}"
+        if "mean" in tol:
+            assert st["mean"] <= tol["mean"], f"{what} {k}: mean {st['mean']:.3g}"
+    print("\nBWD", what, {k: f"{v['max']:.1e}/{v['mean']:.1e}" for k, v in report.items()})
+
+
+@pytest.mark.parametrize("euler", [False, True])
+@pytest.mark.parametrize("opt", [True, False])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward(euler, opt, io):
+    _check(io, batch=2, L=301, dim=136, N=16, euler=euler, opt=opt,
+           what=f"bwd {io} euler={euler} opt={opt}")
+
+
+@pytest.mark.parametrize("N,dim,L", [(5, 37, 64), (1, 40, 17), (8, 200, 33)])
+def test_backward_small_state_and_ragged(N, dim, L):
+    _check("f32", batch=3, L=L, dim=dim, N=N, euler=False, opt=True, what=f"bwd N={N} dim={dim}")
+
+
+def test_backward_is_deterministic():
+    w, x, dy, dh, h0, softplus = _case("bf16", 2, 200, 136, 16, False, True)
+    run = lambda: binding.bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], dy, D=x["D"],  # noqa
+                              z=x["z"], delta_bias=x["delta_bias"], dh_last=dh, h0=h0,
+                              want_dh0=True)
+    a, b = run(), run()
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
