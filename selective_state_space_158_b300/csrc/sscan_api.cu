@@ -40,6 +40,14 @@ unsigned int* status_word(int dev) {
   return s.status;
 }
 
+// The TMA-staged kernel when the arguments allow it, else the plain-load kernel.
+cudaError_t launch_forward(const sscan::FwdArgs& a) {
+  const char* force = std::getenv("SSCAN_PATH");
+  const bool want_simple = force && std::strcmp(force, "simple") == 0;
+  if (!want_simple && sscan::tma_path_ok(a)) return sscan::launch_tma(a, sscan::tuning_from_env());
+  return sscan::launch_simple(a);
+}
+
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
   if (a < 0 || b < 0) return false;
   if (a != 0 && b > INT64_MAX / a) return false;
@@ -137,14 +145,7 @@ sscan_status_t sscan_fwd_ex(const void* u, const void* delta, const float* A, co
   a.stream = stream;
   a.status = status_word(dev);
   if (!a.status) return SSCAN_ERR_CUDA;
-  cudaError_t e;
-  const char* force = std::getenv("SSCAN_PATH");
-  const bool want_simple = force && std::strcmp(force, "simple") == 0;
-  if (!want_simple && sscan::tma_path_ok(a))
-    e = sscan::launch_tma(a, sscan::tuning_from_env());
-  else
-    e = sscan::launch_simple(a);
-  return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+  return launch_forward(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 
 sscan_status_t sscan_fwd(const void* u, const void* delta, const float* A, const void* B,
@@ -219,6 +220,40 @@ sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const
     }
     return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
   }
+  // Checkpoints: the forward pass (same inputs) writes the state before every 16-step chunk;
+  // its y goes to scratch. Stream-ordered workspace, released after the backward kernels.
+  const int dev = current_device();
+  const size_t es = dtype == SSCAN_F32 ? 4 : 2;
+  const int64_t n_chunks = (L + 15) / 16;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t ck_bytes = up(size_t(n_chunks) * size_t(batch * dim * N) * sizeof(float));
+  const size_t y_bytes = up(size_t(bld) * es);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, ck_bytes + y_bytes, stream) != cudaSuccess) return SSCAN_ERR_CUDA;
+  float* ckpt = static_cast<float*>(ws);
+  sscan::FwdArgs f;
+  f.u = u;
+  f.delta = delta;
+  f.A = A;
+  f.B = B;
+  f.C = C;
+  f.D = D;
+  f.z = z;
+  f.bias = delta_bias;
+  f.softplus = softplus_flag != 0;
+  f.h0 = h0;
+  f.euler = disc == SSCAN_DISC_EULER;
+  f.y = static_cast<char*>(ws) + ck_bytes;
+  f.h_last = nullptr;
+  f.h_ckpt = ckpt;
+  f.batch = batch;
+  f.L = L;
+  f.dim = dim;
+  f.N = N;
+  f.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
+  f.stream = stream;
+  f.status = status_word(dev);
+  cudaError_t e = f.status ? launch_forward(f) : cudaErrorMemoryAllocation;
   sscan::BwdArgs a;
   a.u = u;
   a.delta = delta;
@@ -248,7 +283,10 @@ sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const
   a.N = N;
   a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
   a.stream = stream;
-  return sscan::launch_bwd(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+  a.ckpt = ckpt;
+  if (e == cudaSuccess) e = sscan::launch_bwd(a);
+  const cudaError_t e2 = cudaFreeAsync(ws, stream);
+  return (e == cudaSuccess && e2 == cudaSuccess) ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 
 sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bias,

@@ -8,13 +8,15 @@
 //   d(dt_t) = sum_n lam_t (B_t u_t + h_{t-1} da_t/d(dt)),  dA += lam_t h_{t-1} da_t/dA
 //   ddelta_t = d(dt_t) sigmoid(x_t) (softplus), dz_t = dy_t s_t SiLU'(z_t), dh0 = a_0 lam_0.
 //
-// Three kernels:
-//   1. bwd_ckpt_kernel: the forward recurrence (no readout) writing the state before every
-//      16-step chunk (B * D * N floats per chunk);
-//   2. bwd_chunk_kernel: four lanes per channel (four states each); chunks in reverse order: the
-//      chunk's 16 steps are recomputed from its checkpoint (states kept in registers), then the
-//      adjoint sweeps back through them. Per-channel sums over the four lanes use shuffles. dB
-//      and dC sum over channels: each warp reduces its 8 channels with shuffles into its own
+// Steps:
+//   1. checkpoints: the forward kernel (sscan_fwd_ex's path, with its h_ckpt output) writes the
+//      state before every 16-step chunk (B * D * N floats per chunk);
+//   2. bwd_chunk_kernel: four lanes per channel (four states each); chunks in reverse order. The
+//      chunk's per-(step, channel) values (dt, u, softplus slope, dy, gate and its slope) are
+//      computed once into a double-buffered shared-memory table from inputs loaded a chunk ahead;
+//      the chunk's 16 states are recomputed from its checkpoint in registers, then the adjoint
+//      sweeps back through them. Per-channel sums over the four lanes use shuffles. dB and dC
+//      sum over channels: each warp reduces its 8 channels with shuffles into its own
 //      shared-memory slot, the CTA adds the slots in warp order, and the CTA's partial is
 //      stored per channel group;
 //   3. bwd_reduce_kernel: sums the partials in a fixed order (deterministic): dB, dC over channel
@@ -34,7 +36,7 @@ namespace {
 constexpr int kBT = 16;      // steps per chunk
 constexpr int kBG = 4;       // lanes per channel
 constexpr int kBK = 4;       // states per lane (N <= 16)
-constexpr int kBThreads = 256;
+constexpr int kBThreads = 128;  // three blocks per SM under the 170-register budget
 constexpr int kBCh = kBThreads / kBG;  // channels per CTA
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + ex2(-x * kLog2e)); }
@@ -45,79 +47,33 @@ __device__ __forceinline__ float factor(float dt, float a2) {
   return EULER ? fmaf(dt, a2, 1.f) : ex2(fmaf(dt, a2, kEx2ArgShift));
 }
 
-// ---- 1. checkpoints: the state before every chunk ----------------------------------------------
-template <typename IO, bool EULER>
-__global__ void __launch_bounds__(256) bwd_ckpt_kernel(BwdArgs a, int n_chunks,
-                                                       float* __restrict__ ckpt) {
-  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t c = gid / kBG;  // channel b * dim + d
-  const int g = int(gid % kBG);
-  if (c >= a.batch * a.dim) return;
-  const int64_t b = c / a.dim, d = c - b * a.dim;
-  const int N = int(a.N);
-  const IO* u = static_cast<const IO*>(a.u);
-  const IO* dl = static_cast<const IO*>(a.delta);
-  const IO* Bm = static_cast<const IO*>(a.B);
-  float a2[kBK], h[kBK];
-#pragma unroll
-  for (int k = 0; k < kBK; ++k) {
-    const int n = g * kBK + k;
-    a2[k] = n < N ? a.A[d * N + n] * (EULER ? 1.f : kLog2e) : 0.f;
-    h[k] = (a.h0 && n < N) ? a.h0[c * N + n] : 0.f;
-  }
-  const float bias = a.bias ? a.bias[d] : 0.f;
-  const size_t ck_stride = size_t(a.batch) * a.dim * N;
-  for (int ch = 0; ch < n_chunks; ++ch) {
-#pragma unroll
-    for (int k = 0; k < kBK; ++k) {
-      const int n = g * kBK + k;
-      if (n < N) ckpt[size_t(ch) * ck_stride + size_t(c) * N + n] = h[k];
-    }
-    const int64_t t0 = int64_t(ch) * kBT;
-    float dts[kBT], dtu[kBT];
-#pragma unroll
-    for (int j = 0; j < kBT; ++j) {  // the chunk's inputs first, so the loads overlap
-      const int64_t t = t0 + j;
-      float x = 0.f, uu = 0.f;
-      if (t < a.L) {
-        const int64_t i = (b * a.L + t) * a.dim + d;
-        x = to_f32(dl[i]) + bias;
-        uu = to_f32(u[i]);
-      }
-      const float dt = t < a.L ? (a.softplus ? softplus_f(x) : x) : 0.f;
-      dts[j] = dt;
-      dtu[j] = dt * uu;
-    }
-#pragma unroll
-    for (int j = 0; j < kBT; ++j) {
-      const int64_t t = t0 + j;
-#pragma unroll
-      for (int k = 0; k < kBK; ++k) {
-        const int n = g * kBK + k;
-        const float bt = (t < a.L && n < N) ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
-        h[k] = fmaf(factor<EULER>(dts[j], a2[k]), h[k], dtu[j] * bt);
-      }
-    }
-  }
-}
+// ---- the adjoint sweep over chunks in reverse ------------------------------------------------
+// Per (step, channel) values of a chunk, computed once and shared by the channel's four lanes.
+enum { kPdt = 0, kPu, kPsx, kPdy, kPgz, kPgp, kPs, kPN };  // kPs: readout's state part
+struct BwdSmem {
+  static constexpr size_t slot_pro = size_t(kBT) * kBCh * kPN;   // floats
+  static constexpr size_t slot_bc = size_t(kBT) * 16;             // floats, each of B and C
+  static constexpr size_t slot = slot_pro + 2 * slot_bc;
+  static constexpr size_t red = size_t(kBThreads / 32) * kBT * 16;  // per-warp dB / dC slots
+  static constexpr size_t bytes = (2 * slot + 2 * red) * sizeof(float);
+};
 
-// ---- 2. the adjoint sweep over chunks in reverse -----------------------------------------------
 template <typename IO, bool EULER>
-__global__ void __launch_bounds__(kBThreads, 1) bwd_chunk_kernel(BwdArgs a, int n_chunks,
-                                                                 const float* __restrict__ ckpt,
+__global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int n_chunks,
                                                                  float* __restrict__ part_dB,
                                                                  float* __restrict__ part_dC,
                                                                  float* __restrict__ part_dA,
                                                                  float* __restrict__ part_dD,
                                                                  float* __restrict__ part_db) {
-  // Per-warp slots of the chunk's dB / dC sums over the warp's channels; the CTA adds the
-  // slots in warp order (no atomics: the result does not depend on timing).
-  __shared__ float sdB[kBThreads / 32][kBT][16], sdC[kBThreads / 32][kBT][16];
+  extern __shared__ __align__(16) float bsm[];
+  float* slots = bsm;                          // [2][slot]
+  float* sdB = bsm + 2 * BwdSmem::slot;        // [warp][kBT][16]: per-warp slots, added in warp
+  float* sdC = sdB + BwdSmem::red;             // order (no atomics: timing-independent results)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane % kBG;
+  const int g = lane % kBG, cl = tid / kBG;
   const int64_t b = blockIdx.y;
   const int cg_idx = blockIdx.x;
-  const int64_t d = int64_t(cg_idx) * kBCh + tid / kBG;
+  const int64_t d = int64_t(cg_idx) * kBCh + cl;
   const bool live = d < a.dim;
   const int N = int(a.N);
   const int64_t c = b * a.dim + d;
@@ -142,81 +98,120 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_chunk_kernel(BwdArgs a, int 
   const size_t ck_stride = size_t(a.batch) * a.dim * N;
   const size_t part_stride = size_t(a.batch) * a.L * 16;  // one channel group's [b][t][16]
 
+  // Raw inputs of one chunk for this thread: its channel's own steps j = g + 4 i (delta, u, z,
+  // dy) and one (step, state) element of B and C. Loaded a chunk ahead, so the loads overlap
+  // the previous chunk's work.
+  constexpr int kBC = kBT * 16 / kBThreads;  // B / C elements per thread and chunk
+  float r_dl[kBT / kBG], r_u[kBT / kBG], r_z[kBT / kBG], r_dy[kBT / kBG], r_B[kBC], r_C[kBC];
+  auto prefetch = [&](int ch) {
+    const int64_t t0 = int64_t(ch) * kBT;
+#pragma unroll
+    for (int i = 0; i < kBT / kBG; ++i) {
+      const int64_t t = t0 + g + kBG * i;
+      const bool tv = live && t < a.L;
+      const int64_t idx = (b * a.L + t) * a.dim + d;
+      r_dl[i] = tv ? to_f32(dl[idx]) : 0.f;
+      r_u[i] = tv ? to_f32(u[idx]) : 0.f;
+      r_z[i] = (tv && zz) ? to_f32(zz[idx]) : 0.f;
+      r_dy[i] = tv ? to_f32(dy[idx]) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < kBC; ++e) {
+      const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
+      const int64_t t = t0 + j;
+      const bool ok = t < a.L && n < N;
+      r_B[e] = ok ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
+      r_C[e] = ok ? to_f32(Cm[(b * a.L + t) * N + n]) : 0.f;
+    }
+  };
+  prefetch(n_chunks - 1);
+
   for (int ch = n_chunks - 1; ch >= 0; --ch) {
     const int64_t t0 = int64_t(ch) * kBT;
+    float* sl = slots + size_t(ch & 1) * BwdSmem::slot;
+    float* P = sl;                                // [kBT][kBCh][kPN]
+    float* Bs = sl + BwdSmem::slot_pro;           // [kBT][16]
+    float* Cs = Bs + BwdSmem::slot_bc;
+    // The chunk's per-(step, channel) values: dt, u, sigmoid(x) (softplus slope), dy, SiLU(z),
+    // SiLU'(z); steps past the end get dt = 0 and dy = 0 (an identity step).
+#pragma unroll
+    for (int i = 0; i < kBT / kBG; ++i) {
+      const int j = g + kBG * i;
+      const bool tv = live && t0 + j < a.L;
+      const float x = r_dl[i] + bias;
+      float* pp = P + (size_t(j) * kBCh + cl) * kPN;
+      pp[kPdt] = tv ? (a.softplus ? softplus_f(x) : x) : 0.f;
+      pp[kPu] = r_u[i];
+      pp[kPsx] = a.softplus ? sigmoid_f(x) : 1.f;
+      pp[kPdy] = r_dy[i];
+      if (zz) {
+        const float sg = sigmoid_f(r_z[i]);
+        pp[kPgz] = r_z[i] * sg;
+        pp[kPgp] = sg * fmaf(r_z[i], 1.f - sg, 1.f);
+      } else {
+        pp[kPgz] = 1.f;
+        pp[kPgp] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kBC; ++e) {
+      Bs[tid + e * kBThreads] = r_B[e];
+      Cs[tid + e * kBThreads] = r_C[e];
+    }
+    __syncthreads();
+
     // Recompute the chunk: hist[j] is the state before step t0 + j (hist[kBT]: after the last).
-    float hist[kBT + 1][kBK], dts[kBT], uus[kBT], spart[kBT];
+    float hist[kBT + 1][kBK];
 #pragma unroll
     for (int k = 0; k < kBK; ++k) {
       const int n = g * kBK + k;
-      hist[0][k] = (live && n < N) ? ckpt[size_t(ch) * ck_stride + size_t(c) * N + n] : 0.f;
+      hist[0][k] = (live && n < N) ? a.ckpt[size_t(ch) * ck_stride + size_t(c) * N + n] : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kBT; ++j) {
-      const int64_t t = t0 + j;
-      const bool tv = live && t < a.L;
-      float x = 0.f, uu = 0.f;
-      if (tv) {
-        const int64_t i = (b * a.L + t) * a.dim + d;
-        x = to_f32(dl[i]) + bias;
-        uu = to_f32(u[i]);
-      }
-      const float dt = tv ? (a.softplus ? softplus_f(x) : x) : 0.f;
-      dts[j] = dt;
-      uus[j] = uu;
+      const float* pp = P + (size_t(j) * kBCh + cl) * kPN;
+      const float dt = pp[kPdt], dtu = dt * pp[kPu];
+      const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+      const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+      const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
       float sp = 0.f;
 #pragma unroll
       for (int k = 0; k < kBK; ++k) {
-        const int n = g * kBK + k;
-        const bool nv = tv && n < N;
-        const float bt = nv ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
-        const float ct = nv ? to_f32(Cm[(b * a.L + t) * N + n]) : 0.f;
-        hist[j + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[j][k], dt * uu * bt);
-        sp = fmaf(ct, hist[j + 1][k], sp);
+        hist[j + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[j][k], dtu * bv[k]);
+        sp = fmaf(cv[k], hist[j + 1][k], sp);
       }
-      spart[j] = sp;
+      // The readout's state part summed over the channel's four lanes, kept for the gate's
+      // gradient.
+      sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+      sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+      if (g == 0) P[(size_t(j) * kBCh + cl) * kPN + kPs] = sp;
     }
-    // The readout's state part summed over the channel's four lanes (every lane gets it).
-#pragma unroll
-    for (int j = 0; j < kBT; ++j) {
-      spart[j] += __shfl_xor_sync(0xffffffffu, spart[j], 1);
-      spart[j] += __shfl_xor_sync(0xffffffffu, spart[j], 2);
-    }
+    __syncwarp();
+    if (ch > 0) prefetch(ch - 1);  // the next chunk's inputs, overlapping the adjoint sweep
     // Adjoint sweep back through the chunk.
+    float* wB = sdB + size_t(warp) * kBT * 16;
+    float* wC = sdC + size_t(warp) * kBT * 16;
 #pragma unroll
     for (int j = kBT - 1; j >= 0; --j) {
       const int64_t t = t0 + j;
       const bool tv = live && t < a.L;
-      const float dt = dts[j], uu = uus[j];
-      float dyt = 0.f, zt = 0.f, x = 0.f;
-      if (tv) {
-        const int64_t i = (b * a.L + t) * a.dim + d;
-        dyt = to_f32(dy[i]);
-        if (zz) zt = to_f32(zz[i]);
-        x = to_f32(dl[i]) + bias;
-      }
-      float ds = dyt, dzv = 0.f;
-      if (zz) {
-        const float sg = sigmoid_f(zt);
-        ds = dyt * zt * sg;
-        dzv = dyt * (spart[j] + Dd * uu) * sg * fmaf(zt, 1.f - sg, 1.f);
-      }
+      const float* pp = P + (size_t(j) * kBCh + cl) * kPN;
+      const float dt = pp[kPdt], uu = pp[kPu], dyt = pp[kPdy];
+      const float ds = dyt * pp[kPgz];
+      const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+      const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+      const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
       float ddt = 0.f, dup = 0.f, vB[kBK], vC[kBK];
 #pragma unroll
       for (int k = 0; k < kBK; ++k) {
-        const int n = g * kBK + k;
-        const bool nv = tv && n < N;
-        const float bt = nv ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
-        const float ct = nv ? to_f32(Cm[(b * a.L + t) * N + n]) : 0.f;
         const float fa = factor<EULER>(dt, a2[k]);
-        const float lam = fmaf(ds, ct, mu[k]);
-        const float da = lam * hist[j][k];
-        const float dfa = EULER ? da : da * fa;  // lam h_{t-1} times d(factor)/d(dt A)
-        ddt = fmaf(dfa, Av[k], fmaf(lam * bt, uu, ddt));
+        const float lam = fmaf(ds, cv[k], mu[k]);
+        const float dfa = EULER ? lam * hist[j][k] : lam * hist[j][k] * fa;
+        ddt = fmaf(dfa, Av[k], fmaf(lam * bv[k], uu, ddt));
         dA[k] = fmaf(dfa, dt, dA[k]);
         vB[k] = lam * dt * uu;
         vC[k] = ds * hist[j + 1][k];
-        dup = fmaf(lam * dt, bt, dup);
+        dup = fmaf(lam * dt, bv[k], dup);
         mu[k] = fa * lam;
       }
       // per channel: sum over the four lanes
@@ -226,14 +221,14 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_chunk_kernel(BwdArgs a, int 
       dup += __shfl_xor_sync(0xffffffffu, dup, 2);
       if (tv && g == 0) {
         const int64_t i = (b * a.L + t) * a.dim + d;
-        const float dx = a.softplus ? ddt * sigmoid_f(x) : ddt;
+        const float dx = ddt * pp[kPsx];
         store_io(static_cast<IO*>(a.du) + i, fmaf(ds, Dd, dup));
         store_io(static_cast<IO*>(a.ddelta) + i, dx);
-        if (zz) store_io(static_cast<IO*>(a.dz) + i, dzv);
+        if (zz) store_io(static_cast<IO*>(a.dz) + i, dyt * fmaf(Dd, uu, pp[kPs]) * pp[kPgp]);
         dbias += dx;
         dD = fmaf(ds, uu, dD);
       }
-      // dB, dC: sum over the warp's 8 channels (lanes with the same g), then into the CTA tile
+      // dB, dC: sum over the warp's 8 channels (lanes with the same g) into the warp's slot
 #pragma unroll
       for (int k = 0; k < kBK; ++k) {
 #pragma unroll
@@ -243,31 +238,29 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_chunk_kernel(BwdArgs a, int 
         }
       }
       if (lane < kBG) {
-#pragma unroll
-        for (int k = 0; k < kBK; ++k) {
-          sdB[warp][j][g * kBK + k] = vB[k];
-          sdC[warp][j][g * kBK + k] = vC[k];
-        }
+        *reinterpret_cast<float4*>(wB + j * 16 + g * kBK) = make_float4(vB[0], vB[1], vB[2], vB[3]);
+        *reinterpret_cast<float4*>(wC + j * 16 + g * kBK) = make_float4(vC[0], vC[1], vC[2], vC[3]);
       }
     }
     __syncthreads();
     // The CTA's partial of this chunk (warp slots added in order) to its channel group's slice.
-    for (int i = tid; i < kBT * 16; i += kBThreads) {
-      const int j = i / 16, n = i % 16;
+#pragma unroll
+    for (int e = 0; e < kBC; ++e) {
+      const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
       const int64_t t = t0 + j;
       if (t < a.L && n < N) {
         float sb = 0.f, sc = 0.f;
 #pragma unroll
         for (int w = 0; w < kBThreads / 32; ++w) {
-          sb += sdB[w][j][n];
-          sc += sdC[w][j][n];
+          sb += sdB[(size_t(w) * kBT + j) * 16 + n];
+          sc += sdC[(size_t(w) * kBT + j) * 16 + n];
         }
         const size_t o = size_t(cg_idx) * part_stride + (size_t(b) * a.L + t) * 16 + n;
         part_dB[o] = sb;
         part_dC[o] = sc;
       }
     }
-    __syncthreads();  // the slots are rewritten by the next chunk
+    __syncthreads();  // warp slots and this chunk's table are reused two chunks on
   }
   if (!live) return;
   // dh0 = a_0 lam_0; per-batch-row partials of dA, dD, dbias.
@@ -327,32 +320,29 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups
 
 template <typename IO, bool EULER>
 cudaError_t launch_bwd_typed(const BwdArgs& a) {
+  static_assert((kBT * 16) % kBThreads == 0, "whole B / C elements per thread and chunk");
   const int n_chunks = int((a.L + kBT - 1) / kBT);
   const int n_groups = int((a.dim + kBCh - 1) / kBCh);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t ck = up(size_t(n_chunks) * a.batch * a.dim * a.N * sizeof(float));
   const size_t pbc = up(size_t(n_groups) * a.batch * a.L * 16 * sizeof(float));
   const size_t pa = up(size_t(a.batch) * a.dim * a.N * sizeof(float));
   const size_t pd = up(size_t(a.batch) * a.dim * sizeof(float));
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, ck + 2 * pbc + pa + 2 * pd, a.stream);
+  cudaError_t e = cudaMallocAsync(&ws, 2 * pbc + pa + 2 * pd, a.stream);
   if (e != cudaSuccess) return e;
   char* p = static_cast<char*>(ws);
-  float* ckpt = reinterpret_cast<float*>(p);
-  float* part_dB = reinterpret_cast<float*>(p + ck);
-  float* part_dC = reinterpret_cast<float*>(p + ck + pbc);
-  float* part_dA = reinterpret_cast<float*>(p + ck + 2 * pbc);
-  float* part_dD = reinterpret_cast<float*>(p + ck + 2 * pbc + pa);
-  float* part_db = reinterpret_cast<float*>(p + ck + 2 * pbc + pa + pd);
-  const int64_t lanes = a.batch * a.dim * kBG;
-  bwd_ckpt_kernel<IO, EULER><<<unsigned((lanes + 255) / 256), 256, 0, a.stream>>>(a, n_chunks,
-                                                                                 ckpt);
-  e = cudaGetLastError();
+  float* part_dB = reinterpret_cast<float*>(p);
+  float* part_dC = reinterpret_cast<float*>(p + pbc);
+  float* part_dA = reinterpret_cast<float*>(p + 2 * pbc);
+  float* part_dD = reinterpret_cast<float*>(p + 2 * pbc + pa);
+  float* part_db = reinterpret_cast<float*>(p + 2 * pbc + pa + pd);
+  auto kern = bwd_chunk_kernel<IO, EULER>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(BwdSmem::bytes));
   if (e == cudaSuccess) {
     dim3 grid(unsigned(n_groups), unsigned(a.batch));
-    bwd_chunk_kernel<IO, EULER><<<grid, kBThreads, 0, a.stream>>>(a, n_chunks, ckpt, part_dB,
-                                                                  part_dC, part_dA, part_dD,
-                                                                  part_db);
+    kern<<<grid, kBThreads, BwdSmem::bytes, a.stream>>>(a, n_chunks, part_dB, part_dC, part_dA,
+                                                        part_dD, part_db);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {

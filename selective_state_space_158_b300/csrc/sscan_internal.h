@@ -25,6 +25,7 @@ struct FwdArgs {
   int euler = 0;              // decay factor 1 + dt A instead of exp(dt A)
   void* y;
   float* h_last;        // nullable
+  float* h_ckpt = nullptr;  // backward pass: state before every 16-step chunk, nullable
   int64_t batch, L, dim, N;
   Io io;
   cudaStream_t stream;
@@ -92,6 +93,7 @@ struct BwdArgs {
   int euler;
   const void* dy;       // (batch, L, dim) io
   const float* dh_last; // nullable
+  const float* ckpt;    // state before every 16-step chunk [n_chunks][batch][dim][N]
   void* du;             // (batch, L, dim) io
   void* ddelta;         // (batch, L, dim) io
   float* dA;            // (dim, N)

@@ -41,8 +41,8 @@ __global__ void __launch_bounds__(128) sscan_simple_kernel(
     const IO* __restrict__ u, const IO* __restrict__ delta, const float* __restrict__ A,
     const IO* __restrict__ Bm, const IO* __restrict__ Cm, const float* __restrict__ Dskip,
     const IO* __restrict__ z, const float* __restrict__ bias, int softplus,
-    const float* __restrict__ h0, IO* __restrict__ y, float* __restrict__ h_last, int64_t batch,
-    int64_t L, int64_t dim, int N) {
+    const float* __restrict__ h0, IO* __restrict__ y, float* __restrict__ h_last,
+    float* __restrict__ h_ckpt, int64_t batch, int64_t L, int64_t dim, int N) {
   const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= batch * dim) return;
   const int64_t b = c / dim, d = c - b * dim;
@@ -55,6 +55,12 @@ __global__ void __launch_bounds__(128) sscan_simple_kernel(
   const float bs = bias ? bias[d] : 0.f;
   const float Dd = Dskip ? Dskip[d] : 0.f;
   for (int64_t t = 0; t < L; ++t) {
+    if (h_ckpt && t % 16 == 0) {  // the state before every 16-step chunk (backward pass)
+      float* dst = h_ckpt + ((t / 16) * batch * dim + c) * N;
+#pragma unroll
+      for (int n = 0; n < kNP; ++n)
+        if (n < N) dst[n] = h[n];
+    }
     const int64_t idx = (b * L + t) * dim + d;
     const float x = to_f32(delta[idx]) + bs;
     const float dt = softplus ? softplus_f(x) : x;
@@ -113,6 +119,7 @@ struct LaneParams {
   const float* bias;
   const float* h0;       // initial state (batch, dim, N), or null for zero
   float* h_last;
+  float* h_ckpt;         // state before every 16-step chunk [n_chunks][batch][dim][N], or null
   unsigned int* status;
   int L, dim, N, batch;
   int softplus, has_z;
@@ -397,6 +404,15 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
         break;
       }
 
+      if (readout && p.h_ckpt && live) {  // the state before this chunk (backward pass)
+        float* dst = p.h_ckpt + ((size_t(c) * p.batch + b) * p.dim + cg) * N;
+#pragma unroll
+        for (int r = 0; r < KP; ++r) {
+          const int n = n0 + 2 * r;
+          if (n < N) dst[n] = h[r].x;
+          if (n + 1 < N) dst[n + 1] = h[r].y;
+        }
+      }
       const IO* u_s = reinterpret_cast<const IO*>(stage_ptr(s, 0)) + cl;
       const IO* dl_s = reinterpret_cast<const IO*>(stage_ptr(s, 1)) + cl;
       const IO* z_s = reinterpret_cast<const IO*>(stage_ptr(s, 2)) + cl;
@@ -737,6 +753,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   p.bias = a.bias;
   p.h0 = a.h0;
   p.h_last = a.h_last;
+  p.h_ckpt = a.h_ckpt;
   p.status = a.status;
   p.L = int(a.L);
   p.dim = int(a.dim);
@@ -877,7 +894,7 @@ cudaError_t launch_simple_typed(const FwdArgs& a) {
       static_cast<const IO*>(a.u), static_cast<const IO*>(a.delta), a.A,
       static_cast<const IO*>(a.B), static_cast<const IO*>(a.C), a.D,
       static_cast<const IO*>(a.z), a.bias, a.softplus, a.h0, static_cast<IO*>(a.y), a.h_last,
-      a.batch, a.L, a.dim, int(a.N));
+      a.h_ckpt, a.batch, a.L, a.dim, int(a.N));
   return cudaGetLastError();
 }
 
