@@ -207,6 +207,25 @@ def dist_setup(n_gpus):
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (all-reduce MAX over the default process group); x itself
+    for a single process. The bench takes the slowest rank's time."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank (weak scaling: every rank runs a
+    full replica)."""
+    return world * units_per_rank / seconds
+
+
 def cpu_baseline(w, x, seconds: float):
     """The oracle, as it stands, on a bounded sample of the workload: whole batch rows (or the
     first k channels of row 0) over the full sequence, sized for about `seconds` of wall time."""
@@ -587,12 +606,9 @@ def main():
         remeasured = True
     if binding.device_error(stream) != 0:
         raise RuntimeError("device-side error during the timed region")
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     sec_per_step = ms_max / 1e3 / args.steps
-    value = world * w.elems / sec_per_step
+    value = whole_job_rate(w.elems, world, sec_per_step)
 
     # ---- roofline of the (only) kernel: one launch per step, timed on its own stream ----
     hbm_gbs, sm_max_mhz, peak_src = peaks()
@@ -650,16 +666,13 @@ def main():
         for _ in range(K2):
             e2e_step()
         el = time.perf_counter() - t0
-        te = torch.tensor([el], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        el = float(te.item())
+        el = max_over_ranks(el, world, dev)
         es = 4 if w.io == "f32" else 2
         bld, bln = w.batch * w.L * w.dim, w.batch * w.L * w.N
         h2d = bld * es * (2 + int(w.has_z)) + 2 * bln * es + w.dim * w.N * 4 + \
             w.dim * 4 * (int(w.has_D) + int(w.has_bias))
         d2h = bld * es + w.batch * w.dim * w.N * 4
-        line["e2e"] = {"value": world * w.elems * K2 / el, "unit": UNIT,
+        line["e2e"] = {"value": whole_job_rate(w.elems * K2, world, el), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "steps": K2, "ms_per_step": el / K2 * 1e3,
                        "api": "sscan_fwd_host (pinned host buffers, copies inside the region)"}
