@@ -275,10 +275,10 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
   const uint32_t tile_bytes = uint32_t(TC) * CH * sizeof(IO);
   const uint32_t bc_bytes = uint32_t(TC) * kNP * sizeof(float);
   const uint32_t stage_bytes = (p.has_z ? 3u : 2u) * tile_bytes + 2u * bc_bytes;
-  // Load q (0 .. n_loads-1) brings chunk c_begin + q % nch into stage q % S.
-  auto issue_load = [&](int q) {
-    const int s = q % S;
-    const int t0 = (c_begin + q % nch) * TC;
+  // Load q (0 .. n_loads-1) brings chunk c_begin + q % nch into stage s = q % S (the caller
+  // passes s; loads past the first pass wrap around to the segment's first chunk).
+  auto issue_load = [&](int q, int s) {
+    const int t0 = (c_begin + (q < nch ? q : q - nch)) * TC;
     mbar_arrive_expect_tx(&full[s], stage_bytes);
     tma_load_3d(stage_ptr(s, 0), &tm_u, ch0, t0, b, &full[s]);
     tma_load_3d(stage_ptr(s, 1), &tm_dl, ch0, t0, b, &full[s]);
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
       done[s] = 0;
       if (q + S < n_loads) {
         fence_smem_to_async();
-        issue_load(q + S);
+        issue_load(q + S, s);
       }
     }
   };
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
   }
   __syncthreads();
   if (tid == 0)
-    for (int q = 0; q < S && q < n_loads; ++q) issue_load(q);
+    for (int q = 0; q < S && q < n_loads; ++q) issue_load(q, q);
 
   const int warp = tid >> 5, lane = tid & 31;
   const int cl = warp * CPW + lane / G;  // channel within the CTA
@@ -345,6 +345,8 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
   bool timed_out = false;
   float sd = 0.f, sd_c = 0.f;  // Kahan sum of this segment's steps (pass 1)
   int q = 0;                   // loads consumed
+  int s = 0;                   // its stage, q % S
+  uint32_t phase = 0;          // parity of the stage's fill, (q / S) & 1
   int ystores = 0;             // y tiles this warp has stored
   const size_t unit = ((size_t(seg) * p.batch + b) * p.n_cg + cgi) * W + warp;
   const size_t units_per_seg = size_t(p.batch) * p.n_cg * W;
@@ -393,12 +395,11 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
         h[r] = __ffma2_rn(accP[r], hz[r], accH[r]);
       }
     }
-    for (int ci = 0; ci < nch; ++ci, ++q) {
+    for (int ci = 0; ci < nch; ++ci, ++q, s = (s + 1 == S) ? 0 : s + 1, phase ^= (s == 0)) {
       const int c = c_begin + ci;
-      const int s = q % S;
       const int t0 = c * TC;
       const int t_valid = min(TC, p.L - t0);
-      const bool landed = mbar_wait_bounded(&full[s], (q / S) & 1, kWaitNs);
+      const bool landed = mbar_wait_bounded(&full[s], phase, kWaitNs);
       if (__any_sync(0xffffffffu, !landed)) {  // warp-uniform: the whole warp leaves
         timed_out = true;
         break;
