@@ -44,6 +44,7 @@ struct TmaTuning {
   int segments = 0;           // time segments run by different CTAs (chunk carry)
   int threads = 0;            // threads per CTA (multiple of 32, <= 256)
   int stages = 0;             // TMA pipeline depth
+  int chunk = 0;              // steps per chunk with four lanes per channel (16 or 32)
 };
 
 // Size checks shared by the C entry points; fills the element counts (batch*L*dim, batch*L*N).
@@ -109,7 +110,8 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd(const BwdArgs& a);
 
-// Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS from the environment (0: unset).
+// Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS / SSCAN_TC from the environment
+// (0: unset).
 TmaTuning tuning_from_env();
 
 }  // namespace sscan

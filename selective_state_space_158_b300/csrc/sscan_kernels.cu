@@ -206,13 +206,17 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_shared(unsigned* p, unsigne
   return old;
 }
 
-// Register budget: up to 255 registers with one or two lanes per channel; with four there are
-// more warps to keep resident, so at most 128.
-template <int G>
-__host__ __device__ constexpr int lane_min_blocks() { return G == 4 ? 2 : 1; }
+// Launch bounds: up to 256 threads and 255 registers with one or two lanes per channel; with
+// four there are more warps to keep resident: at most 128 registers with 16-step chunks, and
+// 128-thread CTAs at 170 registers (three per SM) with 32-step chunks.
+template <int G, int TC>
+__host__ __device__ constexpr int lane_max_threads() { return (G == 4 && TC == 32) ? 128 : 256; }
+template <int G, int TC>
+__host__ __device__ constexpr int lane_min_blocks() { return G == 4 ? (TC == 32 ? 3 : 2) : 1; }
 
 template <typename IO, int G, int TC, bool EULER>
-__global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
+__global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, TC>())
+    sscan_lane_kernel(
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
     const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
@@ -446,21 +450,42 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
         own_u[k] = u2.x;
         own_u[k + 1] = u2.y;
       }
-      float2 dtp[TC], dtup[TC];
+      // With four lanes per channel dt and dt u stay scalars (scalar FMAs cost the same
+      // dispatch cycles as paired ones and need no duplicated pairs, which leaves registers for
+      // longer chunks); otherwise they are duplicated pairs for the packed FMAs.
+      constexpr int NPAIR = kShare ? 1 : TC;
+      float2 dtp[NPAIR], dtup[NPAIR];
+      float dts[kShare ? TC : 1], dus[kShare ? TC : 1];
 #pragma unroll
       for (int t = 0; t < TC; ++t) {
-        float dt, du;
         if constexpr (kShare) {  // step t belongs to lane t % G of this channel's group
           const int src = (lane & ~(G - 1)) | (t % G);
-          dt = __shfl_sync(0xffffffffu, own_dt[t / G], src);
-          du = __shfl_sync(0xffffffffu, own_du[t / G], src);
+          dts[t] = __shfl_sync(0xffffffffu, own_dt[t / G], src);
+          dus[t] = __shfl_sync(0xffffffffu, own_du[t / G], src);
         } else {
-          dt = own_dt[t];
-          du = own_du[t];
+          dtp[t] = f2(own_dt[t], own_dt[t]);
+          dtup[t] = f2(own_du[t], own_du[t]);
         }
-        dtp[t] = f2(dt, dt);
-        dtup[t] = f2(du, du);
       }
+      // dA argument and input term of state pair r at step t.
+      auto arg_at = [&](int t, int r) -> float2 {
+        if constexpr (kShare)
+          return f2(fmaf(dts[t], A2[r].x, kArg), fmaf(dts[t], A2[r].y, kArg));
+        else
+          return __ffma2_rn(dtp[t], A2[r], f2(kArg, kArg));
+      };
+      auto in_at = [&](int t, float2 bb) -> float2 {
+        if constexpr (kShare)
+          return f2(dus[t] * bb.x, dus[t] * bb.y);
+        else
+          return __fmul2_rn(dtup[t], bb);
+      };
+      auto dt_at = [&](int t) -> float {
+        if constexpr (kShare)
+          return dts[t];
+        else
+          return dtp[t].x;
+      };
 #pragma unroll
       for (int k = 0; k < OWN; ++k) {
         if constexpr (kShare || G == 1)
@@ -475,16 +500,16 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
 #pragma unroll
         for (int t = 0; t < TC; ++t) {
           const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
-          csum += dtp[t].x;
+          csum += dt_at(t);
 #pragma unroll
           for (int qq = 0; qq < K / 4; ++qq) {
             const float4 bq = Bq[qq];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int r = 2 * qq + j;
-              const float2 dA = decay(__ffma2_rn(dtp[t], A2[r], f2(kArg, kArg)));
+              const float2 dA = decay(arg_at(t, r));
               const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
-              h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
+              h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
               if constexpr (EULER) Pr[r] = __fmul2_rn(Pr[r], dA);
             }
           }
@@ -514,10 +539,10 @@ __global__ void __launch_bounds__(256, lane_min_blocks<G>()) sscan_lane_kernel(
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int r = 2 * qq + j;
-            const float2 dA = decay(__ffma2_rn(dtp[t], A2[r], f2(kArg, kArg)));
+            const float2 dA = decay(arg_at(t, r));
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
-            h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(dtup[t], bb));
+            h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
             acc[r % NACC] = __ffma2_rn(cc, h[r], acc[r % NACC]);
           }
         }
@@ -747,7 +772,8 @@ cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Works
 
 // Common launch parameters; segments: time segments requested (0: automatic, for `units_per_seg`
 // warp units of state).
-LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64_t units_per_seg) {
+LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64_t units_per_seg,
+                       int TC = kLaneTC) {
   LaneParams p;
   p.A = a.A;
   p.D = a.D;
@@ -762,7 +788,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   p.batch = int(a.batch);
   p.softplus = a.softplus;
   p.has_z = a.z != nullptr;
-  p.n_chunks = int((a.L + kLaneTC - 1) / kLaneTC);
+  p.n_chunks = int((a.L + TC - 1) / TC);
   p.n_cg = int((a.dim + CH - 1) / CH);
   p.stages = stages;
   // Chunk carry: split the sequence when too few warps would run otherwise (about 2 per SM),
@@ -782,7 +808,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   return p;
 }
 
-template <typename IO, int G, bool EULER>
+template <typename IO, int G, int TC, bool EULER>
 cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
   constexpr int CPW = 32 / G;
   constexpr int K = kNP / G;
@@ -791,14 +817,14 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   const int es = a.io == Io::F32 ? 4 : 2;
   if (stages < 2 || stages > 8) stages = 3;
   while (stages > 2 &&
-         LaneSmem(kLaneTC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
+         LaneSmem(TC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
     --stages;
-  const LaneSmem lay(kLaneTC, W, CPW, es, stages);
+  const LaneSmem lay(TC, W, CPW, es, stages);
   const size_t smem_bytes = lay.total + 128;
   if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
   const int64_t n_cg = (a.dim + CH - 1) / CH;
   const int64_t warps_per_seg = a.batch * n_cg * W;
-  LaneParams p = base_params(a, CH, stages, segments, warps_per_seg);
+  LaneParams p = base_params(a, CH, stages, segments, warps_per_seg, TC);
 
   Workspace w;
   cudaError_t e = prepare_workspace(a, p.n_seg > 1 ? size_t(p.n_seg) * warps_per_seg : 0, K, &w);
@@ -809,14 +835,14 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
 
   CUtensorMap mu, md, mz, mB, mC, my;
   const uint64_t dim = a.dim, L = a.L, bt = a.batch;
-  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&md, a.delta, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, kLaneTC) &&
-            make_map(&mB, w.B16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
-            make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, kLaneTC) &&
-            make_map(&my, a.y, a.io, dim, L, bt, CPW, kLaneTC);
+  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, CH, TC) &&
+            make_map(&md, a.delta, a.io, dim, L, bt, CH, TC) &&
+            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, CH, TC) &&
+            make_map(&mB, w.B16, Io::F32, kNP, L, bt, kNP, TC) &&
+            make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, TC) &&
+            make_map(&my, a.y, a.io, dim, L, bt, CPW, TC);
   if (!ok) return w.release(cudaErrorInvalidValue);
-  auto kern = sscan_lane_kernel<IO, G, kLaneTC, EULER>;
+  auto kern = sscan_lane_kernel<IO, G, TC, EULER>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return w.release(e);
   if (p.n_seg > 1) {
@@ -829,11 +855,16 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   return w.release(cudaGetLastError());
 }
 
+// Chunk length: 32 steps with four lanes per channel (their per-chunk fixed cost is spread over
+// few state updates per step), else 16; always 16 when the backward pass wants checkpoints.
 template <typename IO, bool EULER>
-cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int segments) {
-  if (G == 1) return launch_lane_typed<IO, 1, EULER>(a, threads, stages, segments);
-  if (G == 2) return launch_lane_typed<IO, 2, EULER>(a, threads, stages, segments);
-  return launch_lane_typed<IO, 4, EULER>(a, threads, stages, segments);
+cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int segments,
+                          int chunk) {
+  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, stages, segments);
+  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, stages, segments);
+  const bool long_chunks = !a.h_ckpt && chunk != 16 && threads <= 128;
+  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, stages, segments)
+                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, stages, segments);
 }
 
 }  // namespace
@@ -841,7 +872,7 @@ cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int 
 cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
   // Layout from the number of channels (batch x dim), measured on B300: one lane per channel
   // (16 states per lane, 256-thread CTAs) from about 24k channels up; two lanes (128 threads)
-  // from about 16k; four lanes (128 threads) below that. When the sequence will be split into
+  // from about 16k; four lanes (64 threads, 32-step chunks) below that. When the sequence will be split into
   // time segments anyway (too few warps even with four lanes), one lane per channel again.
   const int64_t chans = a.batch * a.dim;
   int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
@@ -849,17 +880,17 @@ cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
     G = chans >= 24576 ? 1 : (chans >= 16384 ? 2 : 4);
     if (chans * 4 / 32 < kSplitBelowWarps) G = 1;
   }
-  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : 128);
+  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
   if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
-  const int st = tune.stages, sg = tune.segments;
-  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg)
-                                      : launch_lane_g<float, false>(a, G, threads, st, sg);
+  const int st = tune.stages, sg = tune.segments, tc = tune.chunk;
+  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg, tc)
+                                      : launch_lane_g<float, false>(a, G, threads, st, sg, tc);
   using bf = __nv_bfloat16;
-  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg)
-                 : launch_lane_g<bf, false>(a, G, threads, st, sg);
+  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg, tc)
+                 : launch_lane_g<bf, false>(a, G, threads, st, sg, tc);
 }
 
 TmaTuning tuning_from_env() {
@@ -868,6 +899,7 @@ TmaTuning tuning_from_env() {
   t.segments = env_int("SSCAN_SEGMENTS");
   t.threads = env_int("SSCAN_THREADS");
   t.stages = env_int("SSCAN_STAGES");
+  t.chunk = env_int("SSCAN_TC");
 
   return t;
 }
