@@ -523,16 +523,15 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       }
 
       // Pass 2 (or the only pass): ZOH decay on the SFU, packed f32x2 FMAs for the state and
-      // the readout (four partial sums keep the dependency chains short).
+      // the readout.
       float ys[TC];
 #pragma unroll
       for (int t = 0; t < TC; ++t) {
         const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
         const float4* Cq = reinterpret_cast<const float4*>(Cs + t * kNP + n0);
-        constexpr int NACC = KP < 4 ? KP : 4;  // independent partial sums of the readout
-        float2 acc[NACC];
-#pragma unroll
-        for (int i = 0; i < NACC; ++i) acc[i] = f2(0.f, 0.f);
+        // One chain of packed FMAs per step for the readout: the steps of the unrolled chunk
+        // are independent, so a longer chain costs no stall and saves the adds of partial sums.
+        float2 acc = f2(0.f, 0.f);
 #pragma unroll
         for (int qq = 0; qq < K / 4; ++qq) {
           const float4 bq = Bq[qq], cq = Cq[qq];
@@ -543,15 +542,10 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
             h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
-            acc[r % NACC] = __ffma2_rn(cc, h[r], acc[r % NACC]);
+            acc = __ffma2_rn(cc, h[r], acc);
           }
         }
-        float2 a2;
-        if constexpr (NACC == 4)
-          a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        else
-          a2 = __fadd2_rn(acc[0], acc[1]);
-        ys[t] = a2.x + a2.y;
+        ys[t] = acc.x + acc.y;
       }
 
       // Epilogue on this lane's own steps, two at a time: (readout + D u) * SiLU(z) into the
