@@ -16,9 +16,9 @@
 //      computed once into a double-buffered shared-memory table from inputs loaded a chunk ahead;
 //      the chunk's 16 states are recomputed from its checkpoint in registers, then the adjoint
 //      sweeps back through them. Per-channel sums over the four lanes use shuffles. dB and dC
-//      sum over channels: each warp reduces its 8 channels with shuffles into its own
-//      shared-memory slot, the CTA adds the slots in warp order, and the CTA's partial is
-//      stored per channel group;
+//      sum over channels: each warp reduces its 8 channels with a transposing shuffle
+//      reduction into its own shared-memory slot, the CTA adds the slots in warp order, and the
+//      CTA's partial is stored per channel group;
 //   3. bwd_reduce_kernel: sums the partials in a fixed order (deterministic): dB, dC over channel
 //      groups, dA, dD, dbias over batch rows.
 #include <cuda_bf16.h>
@@ -60,6 +60,8 @@ struct BwdSmem {
 
 template <typename IO, bool EULER>
 __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int n_chunks,
+                                                                 int n_groups,
+                                                                 unsigned* __restrict__ tiles,
                                                                  float* __restrict__ part_dB,
                                                                  float* __restrict__ part_dC,
                                                                  float* __restrict__ part_dA,
@@ -71,8 +73,18 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
   float* sdC = sdB + BwdSmem::red;             // order (no atomics: timing-independent results)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane % kBG, cl = tid / kBG;
-  const int64_t b = blockIdx.y;
-  const int cg_idx = blockIdx.x;
+  // Persistent blocks: each takes (batch row, channel group) tiles from a counter until none
+  // are left, so the last wave does not leave SMs idle.
+  __shared__ unsigned s_tile;
+  const unsigned n_tiles = unsigned(a.batch) * unsigned(n_groups);
+  for (;;) {
+  if (tid == 0) s_tile = atomicAdd(tiles, 1u);
+  __syncthreads();
+  const unsigned tile = s_tile;
+  __syncthreads();  // every thread has read the tile before thread 0 fetches the next
+  if (tile >= n_tiles) break;
+  const int64_t b = tile / unsigned(n_groups);
+  const int cg_idx = int(tile % unsigned(n_groups));
   const int64_t d = int64_t(cg_idx) * kBCh + cl;
   const bool live = d < a.dim;
   const int N = int(a.N);
@@ -228,18 +240,26 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
         dbias += dx;
         dD = fmaf(ds, uu, dD);
       }
-      // dB, dC: sum over the warp's 8 channels (lanes with the same g) into the warp's slot
+      // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
+      // reduction: each round halves the values a lane keeps, so after three rounds lane
+      // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
+      // {dB[0..3], dC[0..3]}, and writes it to the warp's slot.
+      {
+        const bool b0 = (lane & 4) != 0, b1 = (lane & 8) != 0, b2 = (lane & 16) != 0;
+        float r1[4], r2[2];
 #pragma unroll
-      for (int k = 0; k < kBK; ++k) {
-#pragma unroll
-        for (int m = 4; m < 32; m <<= 1) {
-          vB[k] += __shfl_xor_sync(0xffffffffu, vB[k], m);
-          vC[k] += __shfl_xor_sync(0xffffffffu, vC[k], m);
+        for (int i = 0; i < 4; ++i) {
+          const float keep = b0 ? vC[i] : vB[i], send = b0 ? vB[i] : vC[i];
+          r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
-      }
-      if (lane < kBG) {
-        *reinterpret_cast<float4*>(wB + j * 16 + g * kBK) = make_float4(vB[0], vB[1], vB[2], vB[3]);
-        *reinterpret_cast<float4*>(wC + j * 16 + g * kBK) = make_float4(vC[0], vC[1], vC[2], vC[3]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float keep = b1 ? r1[2 + i] : r1[i], send = b1 ? r1[i] : r1[2 + i];
+          r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
+        const float r3 = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        (b0 ? wC : wB)[j * 16 + g * kBK + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = r3;
       }
     }
     __syncthreads();
@@ -262,20 +282,22 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
     }
     __syncthreads();  // warp slots and this chunk's table are reused two chunks on
   }
-  if (!live) return;
-  // dh0 = a_0 lam_0; per-batch-row partials of dA, dD, dbias.
+  if (live) {
+    // dh0 = a_0 lam_0; per-batch-row partials of dA, dD, dbias.
 #pragma unroll
-  for (int k = 0; k < kBK; ++k) {
-    const int n = g * kBK + k;
-    if (n < N) {
-      if (a.dh0) a.dh0[c * N + n] = mu[k];
-      part_dA[(size_t(b) * a.dim + d) * N + n] = dA[k];
+    for (int k = 0; k < kBK; ++k) {
+      const int n = g * kBK + k;
+      if (n < N) {
+        if (a.dh0) a.dh0[c * N + n] = mu[k];
+        part_dA[(size_t(b) * a.dim + d) * N + n] = dA[k];
+      }
+    }
+    if (g == 0) {
+      part_dD[size_t(b) * a.dim + d] = dD;
+      part_db[size_t(b) * a.dim + d] = dbias;
     }
   }
-  if (g == 0) {
-    part_dD[size_t(b) * a.dim + d] = dD;
-    part_db[size_t(b) * a.dim + d] = dbias;
-  }
+  }  // tiles
 }
 
 // ---- 3. fixed-order sums of the partials -------------------------------------------------------
@@ -328,7 +350,7 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
   const size_t pa = up(size_t(a.batch) * a.dim * a.N * sizeof(float));
   const size_t pd = up(size_t(a.batch) * a.dim * sizeof(float));
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, 2 * pbc + pa + 2 * pd, a.stream);
+  cudaError_t e = cudaMallocAsync(&ws, 2 * pbc + pa + 2 * pd + 256, a.stream);
   if (e != cudaSuccess) return e;
   char* p = static_cast<char*>(ws);
   float* part_dB = reinterpret_cast<float*>(p);
@@ -336,13 +358,23 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
   float* part_dA = reinterpret_cast<float*>(p + 2 * pbc);
   float* part_dD = reinterpret_cast<float*>(p + 2 * pbc + pa);
   float* part_db = reinterpret_cast<float*>(p + 2 * pbc + pa + pd);
+  unsigned* tiles = reinterpret_cast<unsigned*>(p + 2 * pbc + pa + 2 * pd);
+  e = cudaMemsetAsync(tiles, 0, sizeof(unsigned), a.stream);
   auto kern = bwd_chunk_kernel<IO, EULER>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(BwdSmem::bytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(BwdSmem::bytes));
+  int per_sm = 0, sms = 0, dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBThreads, BwdSmem::bytes);
   if (e == cudaSuccess) {
-    dim3 grid(unsigned(n_groups), unsigned(a.batch));
-    kern<<<grid, kBThreads, BwdSmem::bytes, a.stream>>>(a, n_chunks, part_dB, part_dC, part_dA,
-                                                        part_dD, part_db);
+    const int64_t n_tiles = int64_t(n_groups) * a.batch;
+    const unsigned grid = unsigned(std::max<int64_t>(
+        1, std::min<int64_t>(n_tiles, int64_t(std::max(per_sm, 1)) * sms)));
+    kern<<<grid, kBThreads, BwdSmem::bytes, a.stream>>>(a, n_chunks, n_groups, tiles, part_dB,
+                                                        part_dC, part_dA, part_dD, part_db);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {

@@ -411,11 +411,19 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
 
       if (readout && p.h_ckpt && live) {  // the state before this chunk (backward pass)
         float* dst = p.h_ckpt + ((size_t(c) * p.batch + b) * p.dim + cg) * N;
+        if (KP % 2 == 0 && (N & 3) == 0) {  // 16-byte stores: n0 and N are multiples of 4
 #pragma unroll
-        for (int r = 0; r < KP; ++r) {
-          const int n = n0 + 2 * r;
-          if (n < N) dst[n] = h[r].x;
-          if (n + 1 < N) dst[n + 1] = h[r].y;
+          for (int r = 0; r + 1 < KP; r += 2)
+            if (n0 + 2 * r < N)
+              *reinterpret_cast<float4*>(dst + n0 + 2 * r) =
+                  make_float4(h[r].x, h[r].y, h[r + 1].x, h[r + 1].y);
+        } else {
+#pragma unroll
+          for (int r = 0; r < KP; ++r) {
+            const int n = n0 + 2 * r;
+            if (n < N) dst[n] = h[r].x;
+            if (n + 1 < N) dst[n + 1] = h[r].y;
+          }
         }
       }
       const IO* u_s = reinterpret_cast<const IO*>(stage_ptr(s, 0)) + cl;
