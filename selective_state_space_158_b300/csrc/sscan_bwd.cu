@@ -34,6 +34,7 @@ namespace sscan {
 namespace {
 
 constexpr int kBT = 16;      // steps per chunk
+constexpr int kBH = kBT / 2; // steps per half-chunk sweep
 constexpr int kBG = 4;       // lanes per channel
 constexpr int kBK = 4;       // states per lane (N <= 16)
 constexpr int kBThreads = 128;  // three blocks per SM under the 170-register budget
@@ -48,31 +49,90 @@ __device__ __forceinline__ float factor(float dt, float a2) {
 }
 
 // ---- the adjoint sweep over chunks in reverse ------------------------------------------------
-// Per (step, channel) values of a chunk, computed once and shared by the channel's four lanes.
-enum { kPdt = 0, kPu, kPsx, kPdy, kPgz, kPgp, kPs, kPN };  // kPs: readout's state part
+// 16-byte asynchronous global -> shared copy; bytes past src_bytes (0 .. 16) are zero-filled and
+// not read.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Shared memory of one CTA, in floats. One chunk's table: per (step, channel) PA = {dt, u, ds,
+// softplus slope} and PB = {dy, SiLU'(z)}, and the chunk's B and C rows widened to 16 states.
+// Each lane's partial sums over its four states, {d(dt), du}, summed per channel after the
+// sweep; the readout's state part per (step, channel); per-warp dB / dC slots; per-warp dD /
+// dbias partials. Then, on the staged path, the raw inputs of the next chunk: delta, u, z, dy
+// tiles [kBT][kBCh], B and C rows [kBT][N], checkpoint [kBCh][N].
+template <typename IO>
 struct BwdSmem {
-  static constexpr size_t slot_pro = size_t(kBT) * kBCh * kPN;   // floats
-  static constexpr size_t slot_bc = size_t(kBT) * 16;             // floats, each of B and C
-  static constexpr size_t slot = slot_pro + 2 * slot_bc;
-  static constexpr size_t red = size_t(kBThreads / 32) * kBT * 16;  // per-warp dB / dC slots
-  static constexpr size_t bytes = (2 * slot + 2 * red) * sizeof(float);
+  static constexpr size_t pa = size_t(kBT) * kBCh * 4;
+  static constexpr size_t pb = size_t(kBT) * kBCh * 2;
+  static constexpr size_t bc = size_t(kBT) * 16;                    // each of B and C
+  static constexpr size_t part2 = size_t(kBG) * kBT * kBCh * 2;     // [g][t][channel]
+  static constexpr size_t part1 = size_t(kBT) * kBCh;               // [t][channel]
+  static constexpr size_t red = size_t(kBThreads / 32) * kBT * 16;  // [warp][t][16]
+  static constexpr size_t ep = size_t(kBThreads / 32) * kBCh * 2;   // [warp][channel]
+  static constexpr size_t base = pa + pb + 2 * bc + part2 + part1 + 2 * red + ep;
+  static constexpr size_t tile_bytes = size_t(kBT) * kBCh * sizeof(IO);  // one io tile
+  static constexpr size_t row_bytes = size_t(kBT) * 16 * sizeof(IO);     // B or C, N <= 16
+  static constexpr size_t ck_bytes = size_t(kBCh) * 16 * sizeof(float);
+  static constexpr size_t stage_bytes = 4 * tile_bytes + 2 * row_bytes + ck_bytes;
+  static constexpr size_t bytes(bool staged) {
+    return base * sizeof(float) + (staged ? stage_bytes : 0);
+  }
 };
 
-template <typename IO, bool EULER>
-__global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int n_chunks,
-                                                                 int n_groups,
-                                                                 unsigned* __restrict__ tiles,
-                                                                 float* __restrict__ part_dB,
-                                                                 float* __restrict__ part_dC,
-                                                                 float* __restrict__ part_dA,
-                                                                 float* __restrict__ part_dD,
-                                                                 float* __restrict__ part_db) {
+// STAGED: the next chunk's inputs are copied into shared memory with cp.async while the current
+// one is processed (needs dim and N rows in whole 16-byte pieces and 16-byte aligned tensors);
+// otherwise each thread loads them into registers a chunk ahead. MINB: resident CTAs per SM the
+// register budget is cut for.
+template <typename IO, bool EULER, bool STAGED, int MINB>
+__global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, int n_chunks,
+                                                                    int n_groups,
+                                                                    unsigned* __restrict__ tiles,
+                                                                    float* __restrict__ part_dB,
+                                                                    float* __restrict__ part_dC,
+                                                                    float* __restrict__ part_dA,
+                                                                    float* __restrict__ part_dD,
+                                                                    float* __restrict__ part_db) {
+  using SM = BwdSmem<IO>;
   extern __shared__ __align__(16) float bsm[];
-  float* slots = bsm;                          // [2][slot]
-  float* sdB = bsm + 2 * BwdSmem::slot;        // [warp][kBT][16]: per-warp slots, added in warp
-  float* sdC = sdB + BwdSmem::red;             // order (no atomics: timing-independent results)
+  float4* PA = reinterpret_cast<float4*>(bsm);              // [kBT][kBCh]
+  float2* PB = reinterpret_cast<float2*>(bsm + SM::pa);     // [kBT][kBCh]
+  float* Bs = bsm + SM::pa + SM::pb;                        // [kBT][16]
+  float* Cs = Bs + SM::bc;
+  float2* R2 = reinterpret_cast<float2*>(Cs + SM::bc);      // [g][t][channel]
+  float* R1 = Cs + SM::bc + SM::part2;                      // [t][channel]
+  float* sdB = R1 + SM::part1;  // [warp][kBT][16]: per-warp slots, added in warp order
+  float* sdC = sdB + SM::red;   // (no atomics: timing-independent results)
+  float2* sep = reinterpret_cast<float2*>(sdC + SM::red);  // [warp][channel]
+  unsigned char* stg = reinterpret_cast<unsigned char*>(bsm + SM::base);
+  const IO* st_io = reinterpret_cast<const IO*>(stg);      // [4][kBT][kBCh]: delta, u, z, dy
+  const IO* st_B = reinterpret_cast<const IO*>(stg + 4 * SM::tile_bytes);
+  const IO* st_C = reinterpret_cast<const IO*>(stg + 4 * SM::tile_bytes + SM::row_bytes);
+  const float* st_ck = reinterpret_cast<const float*>(stg + 4 * SM::tile_bytes + 2 * SM::row_bytes);
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Sweep mapping: lane g of channel cl holds states 4g .. 4g + 3.
   const int g = lane % kBG, cl = tid / kBG;
+  // Output mapping (after the sweep): lane l writes channel l at steps warp + 4 i.
+  const int N = int(a.N);
+  const IO* u = static_cast<const IO*>(a.u);
+  const IO* dl = static_cast<const IO*>(a.delta);
+  const IO* Bm = static_cast<const IO*>(a.B);
+  const IO* Cm = static_cast<const IO*>(a.C);
+  const IO* zz = static_cast<const IO*>(a.z);
+  const IO* dy = static_cast<const IO*>(a.dy);
+  const size_t ck_stride = size_t(a.batch) * a.dim * N;
+  const size_t part_stride = size_t(a.batch) * a.L * 16;  // one channel group's [b][t][16]
+  constexpr int kBC = kBT * 16 / kBThreads;  // B / C elements per thread and chunk
+
   // Persistent blocks: each takes (batch row, channel group) tiles from a counter until none
   // are left, so the last wave does not leave SMs idle.
   __shared__ unsigned s_tile;
@@ -85,16 +145,12 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
   if (tile >= n_tiles) break;
   const int64_t b = tile / unsigned(n_groups);
   const int cg_idx = int(tile % unsigned(n_groups));
-  const int64_t d = int64_t(cg_idx) * kBCh + cl;
+  const int64_t ch0 = int64_t(cg_idx) * kBCh;
+  const int64_t d = ch0 + cl;
   const bool live = d < a.dim;
-  const int N = int(a.N);
   const int64_t c = b * a.dim + d;
-  const IO* u = static_cast<const IO*>(a.u);
-  const IO* dl = static_cast<const IO*>(a.delta);
-  const IO* Bm = static_cast<const IO*>(a.B);
-  const IO* Cm = static_cast<const IO*>(a.C);
-  const IO* zz = static_cast<const IO*>(a.z);
-  const IO* dy = static_cast<const IO*>(a.dy);
+  const int64_t d_o = ch0 + lane;  // output mapping's channel
+  const bool live_o = d_o < a.dim;
   float a2[kBK], Av[kBK], mu[kBK], dA[kBK];
 #pragma unroll
   for (int k = 0; k < kBK; ++k) {
@@ -105,161 +161,237 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
     dA[k] = 0.f;
   }
   const float bias = (live && a.bias) ? a.bias[d] : 0.f;
-  const float Dd = (live && a.D) ? a.D[d] : 0.f;
-  float dD = 0.f, dbias = 0.f;
-  const size_t ck_stride = size_t(a.batch) * a.dim * N;
-  const size_t part_stride = size_t(a.batch) * a.L * 16;  // one channel group's [b][t][16]
+  const float D_o = (live_o && a.D) ? a.D[d_o] : 0.f;
+  float dD_o = 0.f, dbias_o = 0.f;
 
-  // Raw inputs of one chunk for this thread: its channel's own steps j = g + 4 i (delta, u, z,
-  // dy) and one (step, state) element of B and C. Loaded a chunk ahead, so the loads overlap
-  // the previous chunk's work.
-  constexpr int kBC = kBT * 16 / kBThreads;  // B / C elements per thread and chunk
-  float r_dl[kBT / kBG], r_u[kBT / kBG], r_z[kBT / kBG], r_dy[kBT / kBG], r_B[kBC], r_C[kBC];
-  auto prefetch = [&](int ch) {
+  // ---- inputs of chunk ch ----
+  // Staged path: 16-byte pieces of every row segment, zero-filled past the sequence, past dim
+  // and past N (those bytes are not read).
+  auto issue_stage = [&](int ch) {
     const int64_t t0 = int64_t(ch) * kBT;
-#pragma unroll
-    for (int i = 0; i < kBT / kBG; ++i) {
-      const int64_t t = t0 + g + kBG * i;
-      const bool tv = live && t < a.L;
-      const int64_t idx = (b * a.L + t) * a.dim + d;
-      r_dl[i] = tv ? to_f32(dl[idx]) : 0.f;
-      r_u[i] = tv ? to_f32(u[idx]) : 0.f;
-      r_z[i] = (tv && zz) ? to_f32(zz[idx]) : 0.f;
-      r_dy[i] = tv ? to_f32(dy[idx]) : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < kBC; ++e) {
-      const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
+    constexpr int PR = int(kBCh * sizeof(IO) / 16);  // pieces per io row
+    const int64_t row_valid = (a.dim - ch0) * int64_t(sizeof(IO));
+    const IO* srcs[4] = {dl, u, zz, dy};
+    for (int p = tid; p < 4 * kBT * PR; p += kBThreads) {
+      const int arr = p / (kBT * PR), j = (p / PR) % kBT, q = p % PR;
+      if (arr == 2 && !zz) continue;
       const int64_t t = t0 + j;
-      const bool ok = t < a.L && n < N;
-      r_B[e] = ok ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
-      r_C[e] = ok ? to_f32(Cm[(b * a.L + t) * N + n]) : 0.f;
+      const int64_t rem = t < a.L ? row_valid - int64_t(q) * 16 : 0;
+      const uint32_t nb = uint32_t(rem <= 0 ? 0 : (rem >= 16 ? 16 : rem));
+      const char* src = reinterpret_cast<const char*>(srcs[arr]);
+      if (nb) src += ((b * a.L + (t < a.L ? t : 0)) * a.dim + ch0) * int64_t(sizeof(IO)) + q * 16;
+      cp_async16(stg + size_t(arr) * SM::tile_bytes + size_t(j) * kBCh * sizeof(IO) + q * 16,
+                 src, nb);
+    }
+    // B and C: the chunk's rows are contiguous, kBT N elements.
+    const int64_t bc_valid = min(int64_t(kBT), a.L - t0) * N * int64_t(sizeof(IO));
+    const int bc_pieces = int((int64_t(kBT) * N * int64_t(sizeof(IO)) + 15) / 16);
+    for (int p = tid; p < 2 * bc_pieces; p += kBThreads) {
+      const int which = p / bc_pieces, q = p % bc_pieces;
+      const int64_t rem = bc_valid - int64_t(q) * 16;
+      const uint32_t nb = uint32_t(rem <= 0 ? 0 : (rem >= 16 ? 16 : rem));
+      const char* src = reinterpret_cast<const char*>(which ? Cm : Bm);
+      if (nb) src += (b * a.L + t0) * N * int64_t(sizeof(IO)) + q * 16;
+      cp_async16(stg + 4 * SM::tile_bytes + size_t(which) * SM::row_bytes + q * 16, src, nb);
+    }
+    // Checkpoint: the CTA's channels' states before the chunk, contiguous.
+    const int64_t ck_valid = min(int64_t(kBCh), a.dim - ch0) * N * int64_t(sizeof(float));
+    const int ck_pieces = int((int64_t(kBCh) * N * 4 + 15) / 16);
+    for (int q = tid; q < ck_pieces; q += kBThreads) {
+      const int64_t rem = ck_valid - int64_t(q) * 16;
+      const uint32_t nb = uint32_t(rem <= 0 ? 0 : (rem >= 16 ? 16 : rem));
+      const char* src = reinterpret_cast<const char*>(a.ckpt);
+      if (nb) src += ((size_t(ch) * a.batch + b) * a.dim + ch0) * N * sizeof(float) + q * 16;
+      cp_async16(stg + 4 * SM::tile_bytes + 2 * SM::row_bytes + q * 16, src, nb);
+    }
+    cp_async_commit();
+  };
+  // Register path: this thread's channel's own steps j = g + 4 i (delta, u, z, dy), one
+  // (step, state) element of B and C, and its states of the checkpoint.
+  float r_dl[STAGED ? 1 : kBT / kBG], r_u[STAGED ? 1 : kBT / kBG], r_z[STAGED ? 1 : kBT / kBG],
+      r_dy[STAGED ? 1 : kBT / kBG], r_B[STAGED ? 1 : kBC], r_C[STAGED ? 1 : kBC],
+      r_ck[STAGED ? 1 : kBK];
+  auto prefetch = [&](int ch) {
+    if constexpr (!STAGED) {
+      const int64_t t0 = int64_t(ch) * kBT;
+#pragma unroll
+      for (int k = 0; k < kBK; ++k) {
+        const int n = g * kBK + k;
+        r_ck[k] = (live && n < N) ? a.ckpt[size_t(ch) * ck_stride + size_t(c) * N + n] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kBT / kBG; ++i) {
+        const int64_t t = t0 + g + kBG * i;
+        const bool tv = live && t < a.L;
+        const int64_t idx = (b * a.L + t) * a.dim + d;
+        r_dl[i] = tv ? to_f32(dl[idx]) : 0.f;
+        r_u[i] = tv ? to_f32(u[idx]) : 0.f;
+        r_z[i] = (tv && zz) ? to_f32(zz[idx]) : 0.f;
+        r_dy[i] = tv ? to_f32(dy[idx]) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < kBC; ++e) {
+        const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
+        const int64_t t = t0 + j;
+        const bool ok = t < a.L && n < N;
+        r_B[e] = ok ? to_f32(Bm[(b * a.L + t) * N + n]) : 0.f;
+        r_C[e] = ok ? to_f32(Cm[(b * a.L + t) * N + n]) : 0.f;
+      }
+    } else {
+      issue_stage(ch);
     }
   };
   prefetch(n_chunks - 1);
+  if constexpr (STAGED) {
+    cp_async_wait_all();
+    __syncthreads();
+  }
 
   for (int ch = n_chunks - 1; ch >= 0; --ch) {
     const int64_t t0 = int64_t(ch) * kBT;
-    float* sl = slots + size_t(ch & 1) * BwdSmem::slot;
-    float* P = sl;                                // [kBT][kBCh][kPN]
-    float* Bs = sl + BwdSmem::slot_pro;           // [kBT][16]
-    float* Cs = Bs + BwdSmem::slot_bc;
-    // The chunk's per-(step, channel) values: dt, u, sigmoid(x) (softplus slope), dy, SiLU(z),
-    // SiLU'(z); steps past the end get dt = 0 and dy = 0 (an identity step).
+    // The chunk's per-(step, channel) values: dt, u, ds = dy SiLU(z), sigmoid(x) (softplus
+    // slope), dy, SiLU'(z); steps past the end get dt = 0 and dy = 0 (an identity step).
+    float ck0[kBK];
 #pragma unroll
     for (int i = 0; i < kBT / kBG; ++i) {
       const int j = g + kBG * i;
       const bool tv = live && t0 + j < a.L;
-      const float x = r_dl[i] + bias;
-      float* pp = P + (size_t(j) * kBCh + cl) * kPN;
-      pp[kPdt] = tv ? (a.softplus ? softplus_f(x) : x) : 0.f;
-      pp[kPu] = r_u[i];
-      pp[kPsx] = a.softplus ? sigmoid_f(x) : 1.f;
-      pp[kPdy] = r_dy[i];
-      if (zz) {
-        const float sg = sigmoid_f(r_z[i]);
-        pp[kPgz] = r_z[i] * sg;
-        pp[kPgp] = sg * fmaf(r_z[i], 1.f - sg, 1.f);
+      float xd, xu, xz, xy;
+      if constexpr (STAGED) {
+        xd = to_f32(st_io[(0 * kBT + j) * kBCh + cl]);
+        xu = to_f32(st_io[(1 * kBT + j) * kBCh + cl]);
+        xz = zz ? to_f32(st_io[(2 * kBT + j) * kBCh + cl]) : 0.f;
+        xy = to_f32(st_io[(3 * kBT + j) * kBCh + cl]);
       } else {
-        pp[kPgz] = 1.f;
-        pp[kPgp] = 0.f;
+        xd = r_dl[i];
+        xu = r_u[i];
+        xz = r_z[i];
+        xy = r_dy[i];
       }
+      const float x = xd + bias;
+      float gz = 1.f, gp = 0.f;
+      if (zz) {
+        const float sg = sigmoid_f(xz);
+        gz = xz * sg;
+        gp = sg * fmaf(xz, 1.f - sg, 1.f);
+      }
+      PA[j * kBCh + cl] = make_float4(tv ? (a.softplus ? softplus_f(x) : x) : 0.f, xu, xy * gz,
+                                      a.softplus ? sigmoid_f(x) : 1.f);
+      PB[j * kBCh + cl] = make_float2(xy, gp);
     }
 #pragma unroll
     for (int e = 0; e < kBC; ++e) {
-      Bs[tid + e * kBThreads] = r_B[e];
-      Cs[tid + e * kBThreads] = r_C[e];
+      const int idx = tid + e * kBThreads;
+      if constexpr (STAGED) {
+        const int j = idx / 16, n = idx % 16;
+        Bs[idx] = n < N ? to_f32(st_B[j * N + n]) : 0.f;
+        Cs[idx] = n < N ? to_f32(st_C[j * N + n]) : 0.f;
+      } else {
+        Bs[idx] = r_B[e];
+        Cs[idx] = r_C[e];
+      }
     }
-    __syncthreads();
-
-    // Recompute the chunk: hist[j] is the state before step t0 + j (hist[kBT]: after the last).
-    float hist[kBT + 1][kBK];
 #pragma unroll
     for (int k = 0; k < kBK; ++k) {
       const int n = g * kBK + k;
-      hist[0][k] = (live && n < N) ? a.ckpt[size_t(ch) * ck_stride + size_t(c) * N + n] : 0.f;
+      if constexpr (STAGED)
+        ck0[k] = n < N ? st_ck[cl * N + n] : 0.f;
+      else
+        ck0[k] = r_ck[k];
     }
-#pragma unroll
-    for (int j = 0; j < kBT; ++j) {
-      const float* pp = P + (size_t(j) * kBCh + cl) * kPN;
-      const float dt = pp[kPdt], dtu = dt * pp[kPu];
-      const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
-      const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
-      const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
-      float sp = 0.f;
-#pragma unroll
-      for (int k = 0; k < kBK; ++k) {
-        hist[j + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[j][k], dtu * bv[k]);
-        sp = fmaf(cv[k], hist[j + 1][k], sp);
-      }
-      // The readout's state part summed over the channel's four lanes, kept for the gate's
-      // gradient.
-      sp += __shfl_xor_sync(0xffffffffu, sp, 1);
-      sp += __shfl_xor_sync(0xffffffffu, sp, 2);
-      if (g == 0) P[(size_t(j) * kBCh + cl) * kPN + kPs] = sp;
-    }
-    __syncwarp();
-    if (ch > 0) prefetch(ch - 1);  // the next chunk's inputs, overlapping the adjoint sweep
-    // Adjoint sweep back through the chunk.
+    __syncthreads();  // table complete; the staging area is free
+    if (ch > 0) prefetch(ch - 1);  // the next chunk's inputs, overlapping this chunk's work
+
+    // Recompute and sweep the chunk in two halves (steps kBH .. kBT - 1, then 0 .. kBH - 1), each
+    // recomputing its states from the checkpoint: a lane keeps kBH + 1 states per slot instead
+    // of kBT + 1, which leaves registers for more resident warps. hist[jj] is the state before
+    // step t0 + j0 + jj.
     float* wB = sdB + size_t(warp) * kBT * 16;
     float* wC = sdC + size_t(warp) * kBT * 16;
 #pragma unroll
-    for (int j = kBT - 1; j >= 0; --j) {
-      const int64_t t = t0 + j;
-      const bool tv = live && t < a.L;
-      const float* pp = P + (size_t(j) * kBCh + cl) * kPN;
-      const float dt = pp[kPdt], uu = pp[kPu], dyt = pp[kPdy];
-      const float ds = dyt * pp[kPgz];
-      const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
-      const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
-      const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
-      float ddt = 0.f, dup = 0.f, vB[kBK], vC[kBK];
+    for (int half = 1; half >= 0; --half) {
+      const int j0 = half * kBH;
+      float hist[kBH + 1][kBK];
 #pragma unroll
-      for (int k = 0; k < kBK; ++k) {
-        const float fa = factor<EULER>(dt, a2[k]);
-        const float lam = fmaf(ds, cv[k], mu[k]);
-        const float dfa = EULER ? lam * hist[j][k] : lam * hist[j][k] * fa;
-        ddt = fmaf(dfa, Av[k], fmaf(lam * bv[k], uu, ddt));
-        dA[k] = fmaf(dfa, dt, dA[k]);
-        vB[k] = lam * dt * uu;
-        vC[k] = ds * hist[j + 1][k];
-        dup = fmaf(lam * dt, bv[k], dup);
-        mu[k] = fa * lam;
+      for (int k = 0; k < kBK; ++k) hist[0][k] = ck0[k];
+#pragma unroll
+      for (int j = 0; j < j0; ++j) {  // advance to step j0 (its readout part is the other half's)
+        const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
+        const float dt = q.x, dtu = dt * q.y;
+        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+        const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+        for (int k = 0; k < kBK; ++k)
+          hist[0][k] = fmaf(factor<EULER>(dt, a2[k]), hist[0][k], dtu * bv[k]);
       }
-      // per channel: sum over the four lanes
-      ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
-      ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
-      dup += __shfl_xor_sync(0xffffffffu, dup, 1);
-      dup += __shfl_xor_sync(0xffffffffu, dup, 2);
-      if (tv && g == 0) {
-        const int64_t i = (b * a.L + t) * a.dim + d;
-        const float dx = ddt * pp[kPsx];
-        store_io(static_cast<IO*>(a.du) + i, fmaf(ds, Dd, dup));
-        store_io(static_cast<IO*>(a.ddelta) + i, dx);
-        if (zz) store_io(static_cast<IO*>(a.dz) + i, dyt * fmaf(Dd, uu, pp[kPs]) * pp[kPgp]);
-        dbias += dx;
-        dD = fmaf(ds, uu, dD);
+#pragma unroll
+      for (int jj = 0; jj < kBH; ++jj) {
+        const int j = j0 + jj;
+        const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
+        const float dt = q.x, dtu = dt * q.y;
+        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+        const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+        const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
+        float sp = 0.f;
+#pragma unroll
+        for (int k = 0; k < kBK; ++k) {
+          hist[jj + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[jj][k], dtu * bv[k]);
+          sp = fmaf(cv[k], hist[jj + 1][k], sp);
+        }
+        // The readout's state part summed over the channel's four lanes (all four store it).
+        sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+        sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+        R1[j * kBCh + cl] = sp;
       }
-      // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
-      // reduction: each round halves the values a lane keeps, so after three rounds lane
-      // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
-      // {dB[0..3], dC[0..3]}, and writes it to the warp's slot.
-      {
-        const bool b0 = (lane & 4) != 0, b1 = (lane & 8) != 0, b2 = (lane & 16) != 0;
-        float r1[4], r2[2];
+      // Adjoint sweep back through the half. No branches and no global stores: the steps of the
+      // unrolled loop overlap, tied only by the lam / mu recurrence.
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float keep = b0 ? vC[i] : vB[i], send = b0 ? vB[i] : vC[i];
-          r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
+      for (int jj = kBH - 1; jj >= 0; --jj) {
+        const int j = j0 + jj;
+        const float4 q = PA[j * kBCh + cl];
+        const float dt = q.x, uu = q.y, ds = q.z, dtu = dt * uu;
+        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+        const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+        const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
+        // s1 = sum_n lam B (gives d(dt) through the input term, u s1, and du, dt s1);
+        // s2 = sum_n A lam h_{t-1} da/d(dt) / A (the decay term of d(dt)).
+        float s1 = 0.f, s2 = 0.f, vB[kBK], vC[kBK];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float keep = b1 ? r1[2 + i] : r1[i], send = b1 ? r1[i] : r1[2 + i];
-          r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        for (int k = 0; k < kBK; ++k) {
+          const float fa = factor<EULER>(dt, a2[k]);
+          const float lam = fmaf(ds, cv[k], mu[k]);
+          mu[k] = fa * lam;
+          // lam h_{t-1} times da/d(dt) / A: a (zero-order hold) or 1 (first order); times dt
+          // it is the dA term.
+          const float dfa = (EULER ? lam : mu[k]) * hist[jj][k];
+          s2 = fmaf(dfa, Av[k], s2);
+          dA[k] = fmaf(dfa, dt, dA[k]);
+          s1 = fmaf(lam, bv[k], s1);
+          vB[k] = lam * dtu;
+          vC[k] = ds * hist[jj + 1][k];
         }
-        const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
-        const float r3 = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        (b0 ? wC : wB)[j * 16 + g * kBK + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = r3;
+        R2[(g * kBT + j) * kBCh + cl] = make_float2(fmaf(uu, s1, s2), dt * s1);
+        // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
+        // reduction: each round halves the values a lane keeps, so after three rounds lane
+        // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
+        // {dB[0..3], dC[0..3]}, and writes it to the warp's slot.
+        {
+          const bool b0 = (lane & 4) != 0, b1 = (lane & 8) != 0, b2 = (lane & 16) != 0;
+          float r1[4], r2[2];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float keep = b0 ? vC[i] : vB[i], send = b0 ? vB[i] : vC[i];
+            r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float keep = b1 ? r1[2 + i] : r1[i], send = b1 ? r1[i] : r1[2 + i];
+            r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          }
+          const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
+          const float r3 = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          (b0 ? wC : wB)[j * 16 + g * kBK + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = r3;
+        }
       }
     }
     __syncthreads();
@@ -280,10 +412,38 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
         part_dC[o] = sc;
       }
     }
-    __syncthreads();  // warp slots and this chunk's table are reused two chunks on
+    // Per-(step, channel) outputs: the four lanes' partials summed in lane order, then
+    // ddelta = d(dt) sigmoid(x), du = ds D + sum_n lam dt B, dz = dy (D u + readout) SiLU'(z).
+    // A warp's store covers 32 consecutive channels of one step.
+#pragma unroll
+    for (int i = 0; i < kBT / (kBThreads / 32); ++i) {
+      const int j = warp + (kBThreads / 32) * i;
+      const int64_t t = t0 + j;
+      float ddt = 0.f, dup = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < kBG; ++gg) {
+        const float2 r = R2[(gg * kBT + j) * kBCh + lane];
+        ddt += r.x;
+        dup += r.y;
+      }
+      const float sp = R1[j * kBCh + lane];
+      const float4 q = PA[j * kBCh + lane];
+      const float2 qb = PB[j * kBCh + lane];
+      if (live_o && t < a.L) {
+        const int64_t o = (b * a.L + t) * a.dim + d_o;
+        const float dx = ddt * q.w;
+        store_io(static_cast<IO*>(a.du) + o, fmaf(q.z, D_o, dup));
+        store_io(static_cast<IO*>(a.ddelta) + o, dx);
+        if (zz) store_io(static_cast<IO*>(a.dz) + o, qb.x * fmaf(D_o, q.y, sp) * qb.y);
+        dbias_o += dx;
+        dD_o = fmaf(q.z, q.y, dD_o);
+      }
+    }
+    if constexpr (STAGED) cp_async_wait_all();  // the next chunk's inputs have landed
+    __syncthreads();  // table, partials and warp slots are reused; staged inputs are visible
   }
   if (live) {
-    // dh0 = a_0 lam_0; per-batch-row partials of dA, dD, dbias.
+    // dh0 = a_0 lam_0; per-batch-row partials of dA.
 #pragma unroll
     for (int k = 0; k < kBK; ++k) {
       const int n = g * kBK + k;
@@ -292,10 +452,20 @@ __global__ void __launch_bounds__(kBThreads, 3) bwd_chunk_kernel(BwdArgs a, int 
         part_dA[(size_t(b) * a.dim + d) * N + n] = dA[k];
       }
     }
-    if (g == 0) {
-      part_dD[size_t(b) * a.dim + d] = dD;
-      part_db[size_t(b) * a.dim + d] = dbias;
+  }
+  // dD and dbias per batch row: the warps' partials added in warp order.
+  sep[warp * kBCh + lane] = make_float2(dD_o, dbias_o);
+  __syncthreads();
+  if (warp == 0 && live_o) {
+    float sD = 0.f, sb = 0.f;
+#pragma unroll
+    for (int w = 0; w < kBThreads / 32; ++w) {
+      const float2 v = sep[w * kBCh + lane];
+      sD += v.x;
+      sb += v.y;
     }
+    part_dD[size_t(b) * a.dim + d_o] = sD;
+    part_db[size_t(b) * a.dim + d_o] = sb;
   }
   }  // tiles
 }
@@ -360,22 +530,38 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
   float* part_db = reinterpret_cast<float*>(p + 2 * pbc + pa + pd);
   unsigned* tiles = reinterpret_cast<unsigned*>(p + 2 * pbc + pa + 2 * pd);
   e = cudaMemsetAsync(tiles, 0, sizeof(unsigned), a.stream);
-  auto kern = bwd_chunk_kernel<IO, EULER>;
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(BwdSmem::bytes));
-  int per_sm = 0, sms = 0, dev = 0;
+  int sms = 0, dev = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBThreads, BwdSmem::bytes);
-  if (e == cudaSuccess) {
-    const int64_t n_tiles = int64_t(n_groups) * a.batch;
+  // Staged inputs need every copied row segment in whole, aligned 16-byte pieces.
+  auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const bool staged = (a.dim * int64_t(sizeof(IO))) % 16 == 0 &&
+                      (a.N * int64_t(sizeof(IO))) % 16 == 0 && al(a.u) && al(a.delta) &&
+                      al(a.dy) && al(a.B) && al(a.C) && (!a.z || al(a.z)) && al(a.ckpt);
+  // Four resident CTAs per SM (a tighter register budget) only when there are tiles for them.
+  const int64_t n_tiles = int64_t(n_groups) * a.batch;
+  const bool four = n_tiles > int64_t(3) * sms;
+  auto launch = [&](auto kern, bool st) -> cudaError_t {
+    const size_t smem = BwdSmem<IO>::bytes(st);
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    int per_sm = 0;
+    if (r == cudaSuccess)
+      r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBThreads, smem);
+    if (r != cudaSuccess) return r;
     const unsigned grid = unsigned(std::max<int64_t>(
         1, std::min<int64_t>(n_tiles, int64_t(std::max(per_sm, 1)) * sms)));
-    kern<<<grid, kBThreads, BwdSmem::bytes, a.stream>>>(a, n_chunks, n_groups, tiles, part_dB,
-                                                        part_dC, part_dA, part_dD, part_db);
-    e = cudaGetLastError();
+    kern<<<grid, kBThreads, smem, a.stream>>>(a, n_chunks, n_groups, tiles, part_dB, part_dC,
+                                              part_dA, part_dD, part_db);
+    return cudaGetLastError();
+  };
+  if (e == cudaSuccess) {
+    if (staged)
+      e = four ? launch(bwd_chunk_kernel<IO, EULER, true, 4>, true)
+               : launch(bwd_chunk_kernel<IO, EULER, true, 3>, true);
+    else
+      e = four ? launch(bwd_chunk_kernel<IO, EULER, false, 4>, false)
+               : launch(bwd_chunk_kernel<IO, EULER, false, 3>, false);
   }
   if (e == cudaSuccess) {
     const int64_t total = a.batch * a.L * a.N + a.dim * a.N + 2 * a.dim;

@@ -92,3 +92,40 @@ def test_backward_is_deterministic():
     torch.cuda.synchronize()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("io,N,dim,batch", [("bf16", 16, 4096, 4), ("f32", 5, 3000, 5)])
+def test_backward_many_tiles(io, N, dim, batch):
+    """More (batch row, channel group) tiles than three CTAs per SM hold: the kernel built for
+    four resident CTAs, on the staged path (bf16, N 16) and the register path (N 5)."""
+    _check(io, batch=batch, L=21, dim=dim, N=N, euler=False, opt=True,
+           what=f"bwd many tiles {io} N={N}")
+
+
+def _misaligned(t):
+    """A contiguous copy of t whose data starts one element past a 16-byte boundary."""
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    out = flat[1:].view(t.shape)
+    out.copy_(t)
+    return out
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward_unaligned_inputs(io):
+    """Inputs that do not start on a 16-byte boundary take the register-load path and give the
+    same gradients as aligned ones."""
+    w, x, dy, dh, h0, softplus = _case(io, 2, 77, 136, 16, False, True)
+    run = lambda xx, dd: binding.bwd(xx["u"], xx["delta"], xx["A"], xx["B"], xx["C"], dd,  # noqa
+                                     D=xx["D"], z=xx["z"], delta_bias=xx["delta_bias"],
+                                     dh_last=dh, h0=h0, want_dh0=True)
+    ref = run(x, dy)
+    xm = dict(x)
+    for k in ("u", "delta", "z", "B", "C"):
+        xm[k] = _misaligned(x[k])
+    got = run(xm, _misaligned(dy))
+    torch.cuda.synchronize()
+    for k in ref:
+        r, gq = ref[k].float(), got[k].float()
+        tol = 1e-5 if (io == "f32" or k not in IO_GRADS) else 1e-2
+        err = ((gq - r).abs().max() / r.abs().max().clamp_min(1e-30)).item()
+        assert err <= tol, f"{k}: {err:.3g}"
