@@ -74,9 +74,11 @@ struct BwdSmem {
   static constexpr size_t pa = size_t(kBT) * kBCh * 4;
   static constexpr size_t pb = size_t(kBT) * kBCh * 2;
   static constexpr size_t bc = size_t(kBT) * 16;                    // each of B and C
-  static constexpr size_t part2 = size_t(kBG) * kBT * kBCh * 2;     // [g][t][channel]
+  static constexpr size_t part2 = size_t(kBT) * kBCh * kBG * 2;     // [t][channel][g]
   static constexpr size_t part1 = size_t(kBT) * kBCh;               // [t][channel]
-  static constexpr size_t red = size_t(kBThreads / 32) * kBT * 16;  // [warp][t][16]
+  // [warp][t][16]; dC's slots start 16 floats past a bank-aligned offset, so the lanes that
+  // store dB and those that store dC hit different banks.
+  static constexpr size_t red = size_t(kBThreads / 32) * kBT * 16 + 16;
   static constexpr size_t ep = size_t(kBThreads / 32) * kBCh * 2;   // [warp][channel]
   static constexpr size_t base = pa + pb + 2 * bc + part2 + part1 + 2 * red + ep;
   static constexpr size_t tile_bytes = size_t(kBT) * kBCh * sizeof(IO);  // one io tile
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
   float2* PB = reinterpret_cast<float2*>(bsm + SM::pa);     // [kBT][kBCh]
   float* Bs = bsm + SM::pa + SM::pb;                        // [kBT][16]
   float* Cs = Bs + SM::bc;
-  float2* R2 = reinterpret_cast<float2*>(Cs + SM::bc);      // [g][t][channel]
+  float2* R2 = reinterpret_cast<float2*>(Cs + SM::bc);      // [t][channel][g]
   float* R1 = Cs + SM::bc + SM::part2;                      // [t][channel]
   float* sdB = R1 + SM::part1;  // [warp][kBT][16]: per-warp slots, added in warp order
   float* sdC = sdB + SM::red;   // (no atomics: timing-independent results)
@@ -171,14 +173,13 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     const int64_t t0 = int64_t(ch) * kBT;
     constexpr int PR = int(kBCh * sizeof(IO) / 16);  // pieces per io row
     const int64_t row_valid = (a.dim - ch0) * int64_t(sizeof(IO));
-    const IO* srcs[4] = {dl, u, zz, dy};
     for (int p = tid; p < 4 * kBT * PR; p += kBThreads) {
       const int arr = p / (kBT * PR), j = (p / PR) % kBT, q = p % PR;
       if (arr == 2 && !zz) continue;
       const int64_t t = t0 + j;
       const int64_t rem = t < a.L ? row_valid - int64_t(q) * 16 : 0;
       const uint32_t nb = uint32_t(rem <= 0 ? 0 : (rem >= 16 ? 16 : rem));
-      const char* src = reinterpret_cast<const char*>(srcs[arr]);
+      const char* src = reinterpret_cast<const char*>(arr == 0 ? dl : arr == 1 ? u : arr == 2 ? zz : dy);
       if (nb) src += ((b * a.L + (t < a.L ? t : 0)) * a.dim + ch0) * int64_t(sizeof(IO)) + q * 16;
       cp_async16(stg + size_t(arr) * SM::tile_bytes + size_t(j) * kBCh * sizeof(IO) + q * 16,
                  src, nb);
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
           vB[k] = lam * dtu;
           vC[k] = ds * hist[jj + 1][k];
         }
-        R2[(g * kBT + j) * kBCh + cl] = make_float2(fmaf(uu, s1, s2), dt * s1);
+        R2[(j * kBCh + cl) * kBG + g] = make_float2(fmaf(uu, s1, s2), dt * s1);
         // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
         // reduction: each round halves the values a lane keeps, so after three rounds lane
         // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
@@ -419,13 +420,9 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     for (int i = 0; i < kBT / (kBThreads / 32); ++i) {
       const int j = warp + (kBThreads / 32) * i;
       const int64_t t = t0 + j;
-      float ddt = 0.f, dup = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < kBG; ++gg) {
-        const float2 r = R2[(gg * kBT + j) * kBCh + lane];
-        ddt += r.x;
-        dup += r.y;
-      }
+      const float4* r4 = reinterpret_cast<const float4*>(R2 + (j * kBCh + lane) * kBG);
+      const float4 ra = r4[0], rb = r4[1];  // {d(dt), du} of lanes 0, 1 and 2, 3
+      const float ddt = ((ra.x + ra.z) + rb.x) + rb.z, dup = ((ra.y + ra.w) + rb.y) + rb.w;
       const float sp = R1[j * kBCh + lane];
       const float4 q = PA[j * kBCh + lane];
       const float2 qb = PB[j * kBCh + lane];
