@@ -315,6 +315,8 @@ sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bia
   a.width = width;
   a.io = dtype == SSCAN_F32 ? sscan::Io::F32 : sscan::Io::BF16;
   a.stream = stream;
+  a.status = status_word(current_device());
+  if (!a.status) return SSCAN_ERR_CUDA;
   return sscan::launch_conv(a) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
 

@@ -13,6 +13,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <cstdlib>
+
 #include "sscan_device.cuh"
 #include "sscan_internal.h"
 
@@ -160,8 +163,222 @@ __global__ void __launch_bounds__(256) conv_scalar_kernel(const IO* __restrict__
   }
 }
 
+// ---- TMA-staged streaming kernel ------------------------------------------------------------
+// Work item: one tile of kTileT steps x kRowBytes of channels of one batch row. A persistent CTA
+// walks its items (item c, c + grid, ...) through a kStages-deep pipeline: one thread loads each
+// item's input tile with its W - 1 step halo by TMA (rows before t = 0 arrive zero-filled), all
+// threads compute from shared memory into an output tile, and the same thread stores it by TMA
+// (rows past L and channels past dim are clipped). Every input byte is read once (plus the halo,
+// 3/64 of a tile for width 4, mostly from L2) and every output byte written once, with several
+// 18 KB loads in flight per CTA.
+constexpr int kTileT = 64;                       // steps per tile
+constexpr int kRowBytes = 256;                   // channel bytes per tile row
+constexpr int kWords = kRowBytes / 4;            // 4-byte words per row: 2 bf16 or 1 fp32 channels
+constexpr int kConvThreads = 256;
+constexpr int kGroups = kConvThreads / kWords;   // step groups per tile
+constexpr int kStepsPerThread = kTileT / kGroups;
+constexpr int kConvStages = 4;
+constexpr int kMaxTmaWidth = 8;
+
+template <typename IO, int W>
+struct ConvTmaSmem {
+  static constexpr int rows_in = kTileT + W - 1;
+  static constexpr size_t in_stage = size_t(rows_in) * kRowBytes;   // multiple of 128
+  static constexpr size_t out_tile = size_t(kTileT) * kRowBytes;
+  static constexpr size_t off_out = kConvStages * in_stage;
+  static constexpr size_t off_bar = off_out + 2 * out_tile;
+  static constexpr size_t bytes = off_bar + kConvStages * 8 + 128;  // + alignment slack
+};
+
+template <typename IO> struct Word;  // one 4-byte word of a row as floats
+template <> struct Word<float> {
+  static constexpr int C = 1;
+  __device__ static void get(const unsigned char* p, float (&v)[1]) {
+    v[0] = *reinterpret_cast<const float*>(p);
+  }
+  __device__ static void put(unsigned char* p, const float (&v)[1]) {
+    *reinterpret_cast<float*>(p) = v[0];
+  }
+};
+template <> struct Word<__nv_bfloat16> {
+  static constexpr int C = 2;
+  __device__ static void get(const unsigned char* p, float (&v)[2]) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    v[0] = f.x;
+    v[1] = f.y;
+  }
+  __device__ static void put(unsigned char* p, const float (&v)[2]) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
+  }
+};
+
+template <typename IO, int W>
+__global__ void __launch_bounds__(kConvThreads) conv_tma_kernel(
+    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+    const float* __restrict__ w, const float* __restrict__ bias, const IO* __restrict__ x_prev,
+    int silu, int64_t batch, int64_t L, int64_t dim, unsigned* status) {
+  using SM = ConvTmaSmem<IO, W>;
+  constexpr int C = Word<IO>::C;            // channels per word
+  constexpr int CT = kRowBytes / sizeof(IO);  // channels per tile
+  extern __shared__ unsigned char conv_smem_raw[];
+  unsigned char* smem =
+      conv_smem_raw + ((128u - (smem_addr(conv_smem_raw) & 127u)) & 127u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::off_bar);
+  const int tid = threadIdx.x;
+  const int wd = tid % kWords, grp = tid / kWords;
+
+  const int64_t n_cb = (dim + CT - 1) / CT, n_tt = (L + kTileT - 1) / kTileT;
+  const int64_t items = batch * n_tt * n_cb;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t n_my = first < items ? (items - first + stride - 1) / stride : 0;
+  // item -> (batch row, time tile, channel block); neighbouring items are neighbouring channel
+  // blocks of one time tile.
+  auto coords = [&](int64_t it, int64_t& b, int64_t& t0, int64_t& c0) {
+    const int64_t item = first + it * stride;
+    c0 = (item % n_cb) * CT;
+    t0 = ((item / n_cb) % n_tt) * kTileT;
+    b = item / (n_cb * n_tt);
+  };
+  auto issue = [&](int64_t it) {
+    int64_t b, t0, c0;
+    coords(it, b, t0, c0);
+    const int s = int(it % kConvStages);
+    mbar_arrive_expect_tx(&full[s], uint32_t(SM::in_stage));
+    tma_load_3d(smem + size_t(s) * SM::in_stage, &tm_x, int(c0), int(t0 - (W - 1)), int(b),
+                &full[s]);
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_y);
+    for (int s = 0; s < kConvStages; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+    for (int64_t it = 0; it < kConvStages && it < n_my; ++it) issue(it);
+  }
+  __syncthreads();
+
+  bool timed_out = false;
+  for (int64_t it = 0; it < n_my; ++it) {
+    const int s = int(it % kConvStages), ob = int(it & 1);
+    const uint32_t parity = uint32_t((it / kConvStages) & 1);
+    const bool landed = mbar_wait_bounded(&full[s], parity, kWaitNs);
+    if (tid == 0 && it >= 2) tma_store_wait_read<1>();  // output tile of two items ago read
+    if (__syncthreads_or(!landed)) {
+      timed_out = true;
+      break;
+    }
+    int64_t b, t0, c0;
+    coords(it, b, t0, c0);
+    // This thread: word wd (channels c0 + C wd ..), steps t0 + grp * kStepsPerThread + i.
+    const int64_t ch = c0 + int64_t(wd) * C;
+    float wk[W][C], bs[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const bool ok = ch + c < dim;
+#pragma unroll
+      for (int j = 0; j < W; ++j) wk[j][c] = ok ? w[(ch + c) * W + j] : 0.f;
+      bs[c] = (ok && bias) ? bias[ch + c] : 0.f;
+    }
+    const unsigned char* in = smem + size_t(s) * SM::in_stage + size_t(wd) * 4;
+    unsigned char* out = smem + SM::off_out + size_t(ob) * SM::out_tile + size_t(wd) * 4;
+    const int r0 = grp * kStepsPerThread;  // first input row of this thread's window
+    float win[W][C];
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) {
+      Word<IO>::get(in + size_t(r0 + j) * kRowBytes, win[j]);
+      // Rows before t = 0 come from x_prev when given (the tile holds zeros there).
+      if (x_prev && t0 == 0 && r0 + j < W - 1) {
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          win[j][c] = ch + c < dim ? to_f32(x_prev[(b * (W - 1) + r0 + j) * dim + ch + c]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kStepsPerThread; ++i) {
+      Word<IO>::get(in + size_t(r0 + i + W - 1) * kRowBytes, win[W - 1]);
+      float o[C];
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        float acc = bs[c];
+#pragma unroll
+        for (int j = 0; j < W; ++j) acc = fmaf(wk[j][c], win[j][c], acc);
+        o[c] = silu_or_id(acc, silu);
+      }
+      Word<IO>::put(out + size_t(r0 + i) * kRowBytes, o);
+#pragma unroll
+      for (int j = 0; j < W - 1; ++j)
+#pragma unroll
+        for (int c = 0; c < C; ++c) win[j][c] = win[j + 1][c];
+    }
+    fence_smem_to_async();
+    __syncthreads();  // output tile complete; input stage s consumed
+    if (tid == 0) {
+      tma_store_3d(&tm_y, smem + SM::off_out + size_t(ob) * SM::out_tile, int(c0), int(t0),
+                   int(b));
+      tma_store_commit();
+      if (it + kConvStages < n_my) issue(it + kConvStages);
+    }
+  }
+  if (tid == 0) {
+    tma_store_wait_all();
+    if (timed_out) {
+      if (status) atomicOr(status, kErrTimeout);
+      // Loads still in flight get a bounded chance to land before shared memory goes away.
+      for (int s = 0; s < kConvStages; ++s) mbar_wait_bounded(&full[s], 0, 100000);
+    }
+  }
+}
+
+template <typename IO, int W>
+cudaError_t launch_conv_tma(const ConvArgs& a) {
+  using SM = ConvTmaSmem<IO, W>;
+  constexpr int CT = kRowBytes / sizeof(IO);
+  CUtensorMap mx, my;
+  if (!make_tensor_map_3d(&mx, a.x, a.io, uint64_t(a.dim), uint64_t(a.L), uint64_t(a.batch), CT,
+                          SM::rows_in) ||
+      !make_tensor_map_3d(&my, a.y, a.io, uint64_t(a.dim), uint64_t(a.L), uint64_t(a.batch), CT,
+                          kTileT))
+    return cudaErrorInvalidValue;
+  auto kern = conv_tma_kernel<IO, W>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(SM::bytes));
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kConvThreads, SM::bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t items = a.batch * ((a.L + kTileT - 1) / kTileT) * ((a.dim + CT - 1) / CT);
+  const unsigned grid =
+      unsigned(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(std::max(per_sm, 1)) * sms)));
+  kern<<<grid, kConvThreads, SM::bytes, a.stream>>>(mx, my, a.w, a.bias,
+                                                    static_cast<const IO*>(a.x_prev), a.silu,
+                                                    a.batch, a.L, a.dim, a.status);
+  return cudaGetLastError();
+}
+
+// TMA needs 16-byte aligned bases and row strides, coordinates within int32.
+bool conv_tma_ok(const ConvArgs& a, int es) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  return a.width <= kMaxTmaWidth && (a.dim * es) % 16 == 0 && al(a.x) && al(a.y) &&
+         a.dim <= INT32_MAX && a.L + kTileT < INT32_MAX && a.batch <= INT32_MAX &&
+         std::getenv("SSCAN_CONV_PLAIN") == nullptr;
+}
+
 template <typename IO>
 cudaError_t launch_conv_typed(const ConvArgs& a) {
+  if (conv_tma_ok(a, int(sizeof(IO)))) {
+    switch (a.width) {
+      case 1: return launch_conv_tma<IO, 1>(a);
+      case 2: return launch_conv_tma<IO, 2>(a);
+      case 3: return launch_conv_tma<IO, 3>(a);
+      case 4: return launch_conv_tma<IO, 4>(a);
+      case 5: return launch_conv_tma<IO, 5>(a);
+      case 6: return launch_conv_tma<IO, 6>(a);
+      case 7: return launch_conv_tma<IO, 7>(a);
+      case 8: return launch_conv_tma<IO, 8>(a);
+      default: break;
+    }
+  }
   constexpr int V = Vec<IO>::V;
   const IO* x = static_cast<const IO*>(a.x);
   const IO* xp = static_cast<const IO*>(a.x_prev);

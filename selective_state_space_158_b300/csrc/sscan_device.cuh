@@ -159,6 +159,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on one mbarrier wait: one second
+constexpr unsigned kErrTimeout = 1u << 4;    // status bit: a bounded wait ran out
+
 // ---- TMA tensor copies (3-D maps: x = fastest dimension) --------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

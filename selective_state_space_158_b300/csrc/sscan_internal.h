@@ -55,6 +55,11 @@ int check_fwd_args(const void* u, const void* delta, const float* A, const void*
 // Status word of the allocation-free entry point on device `dev` (null before its first call).
 unsigned int* noalloc_status_word(int dev);
 
+// A 3-D tiled TMA map over a dense (d2, d1, d0) tensor of io elements (d0 fastest) with box
+// (b0, b1, 1); false if the driver entry point is missing or rejects the map.
+bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint32_t b0, uint32_t b1);
+
 // True if the TMA-staged kernel can serve these arguments (alignment and stride rules of TMA).
 bool tma_path_ok(const FwdArgs& a);
 
@@ -76,6 +81,7 @@ struct ConvArgs {
   int64_t batch, L, dim, width;
   Io io;
   cudaStream_t stream;
+  unsigned int* status = nullptr;  // device status word (bounded-wait timeouts), nullable
 };
 cudaError_t launch_conv(const ConvArgs& a);
 

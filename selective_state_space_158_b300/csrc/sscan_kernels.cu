@@ -30,8 +30,6 @@
 namespace sscan {
 
 constexpr int kNP = 16;          // states held per channel (N <= 16 is zero-padded to 16)
-constexpr uint64_t kWaitNs = 1000000000ull;  // bound on one mbarrier wait: one second
-constexpr unsigned kErrTimeout = 1u << 4;  // status bit: a bounded wait ran out
 
 // ================================================================================================
 // Plain-load kernel: one thread per (batch row, channel), states in registers, sequential in t.
@@ -663,8 +661,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint32_t b0, uint32_t b1) {
+}  // namespace
+
+bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint32_t b0, uint32_t b1) {
   auto enc = get_encode();
   if (!enc) return false;
   const uint64_t es = io == Io::F32 ? 4 : 2;
@@ -677,6 +677,13 @@ bool make_map(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1, 
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool make_map(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t b0, uint32_t b1) {
+  return make_tensor_map_3d(m, ptr, io, d0, d1, d2, b0, b1);
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

@@ -20,16 +20,15 @@ def _conv_ref(x, w, bias, x_prev, silu):
                          None if x_prev is None else to_np_io(x_prev), silu=silu, io=io)
 
 
-@pytest.mark.parametrize("width", [1, 2, 3, 4, 5, 8, 12])
-@pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("dim", [128, 37])
-def test_conv1d_silu(width, io, dim):
-    """Vector path (width <= 8, aligned dim) and the general path (width 12, odd dim), with and
-    without the previous inputs, against the oracle; L spans several 64-step tiles."""
+@pytest.fixture
+def plain_loads(monkeypatch):
+    monkeypatch.setenv("SSCAN_CONV_PLAIN", "1")
+
+
+def _check_conv(width, io, dim, batch=3, L=200, seed=None):
     g = torch.Generator(device=DEV)
-    g.manual_seed(100 + width)
+    g.manual_seed(100 + width if seed is None else seed)
     dt = torch.float32 if io == "f32" else torch.bfloat16
-    batch, L = 3, 200
     x = torch.randn((batch, L, dim), generator=g, device=DEV).to(dt)
     w = torch.randn((dim, width), generator=g, device=DEV) * 0.5
     bias = torch.randn((dim,), generator=g, device=DEV)
@@ -40,6 +39,29 @@ def test_conv1d_silu(width, io, dim):
         r = _conv_ref(x, w, bias, xp, silu)
         res = compare(y, None, r, None, io)
         assert_within(res, io, f"conv width={width} {io} dim={dim} prev={xp is not None}")
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 4, 5, 8, 12])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("dim", [128, 200, 37])
+def test_conv1d_silu(width, io, dim):
+    """TMA-staged tiles (width <= 8, 16-byte rows: dim 128 and 200, the latter with a ragged
+    channel block) and the general path (width 12, odd dim), with and without the previous
+    inputs, against the oracle; L spans several 64-step tiles and ends in a partial one."""
+    _check_conv(width, io, dim)
+
+
+@pytest.mark.parametrize("width", [1, 4, 8])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv1d_silu_plain_load_path(width, io, plain_loads):
+    """The register-window kernel that serves rows TMA cannot address."""
+    _check_conv(width, io, 128)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv1d_silu_many_tiles_per_cta(io):
+    """More tiles than resident CTAs: every CTA cycles its pipeline stages several times."""
+    _check_conv(4, io, 512, batch=4, L=16384, seed=5)
 
 
 def test_conv1d_then_scan_matches_oracle_chain():
