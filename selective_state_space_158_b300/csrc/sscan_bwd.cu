@@ -74,7 +74,7 @@ struct BwdSmem {
   static constexpr size_t pa = size_t(kBT) * kBCh * 4;
   static constexpr size_t pb = size_t(kBT) * kBCh * 2;
   static constexpr size_t bc = size_t(kBT) * 16;                    // each of B and C
-  static constexpr size_t part2 = size_t(kBT) * kBCh * kBG * 2;     // [t][channel][g]
+  static constexpr size_t part2 = size_t(kBT) * kBG * kBCh * 2;     // [t][g][channel ^ swz]
   static constexpr size_t part1 = size_t(kBT) * kBCh;               // [t][channel]
   // [warp][t][16]; dC's slots start 16 floats past a bank-aligned offset, so the lanes that
   // store dB and those that store dC hit different banks.
@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
   float2* PB = reinterpret_cast<float2*>(bsm + SM::pa);     // [kBT][kBCh]
   float* Bs = bsm + SM::pa + SM::pb;                        // [kBT][16]
   float* Cs = Bs + SM::bc;
-  float2* R2 = reinterpret_cast<float2*>(Cs + SM::bc);      // [t][channel][g]
+  // [t][g][slot]: lane g of channel c at slot c ^ 8 (g & 1), so the four lane groups of a
+  // warp's store fall into both halves of the banks.
+  float2* R2 = reinterpret_cast<float2*>(Cs + SM::bc);
   float* R1 = Cs + SM::bc + SM::part2;                      // [t][channel]
   float* sdB = R1 + SM::part1;  // [warp][kBT][16]: per-warp slots, added in warp order
   float* sdC = sdB + SM::red;   // (no atomics: timing-independent results)
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     mu[k] = (live && a.dh_last && n < N) ? a.dh_last[c * N + n] : 0.f;
     dA[k] = 0.f;
   }
-  const float bias = (live && a.bias) ? a.bias[d] : 0.f;
+  const float bias_o = (live_o && a.bias) ? a.bias[d_o] : 0.f;
   const float D_o = (live_o && a.D) ? a.D[d_o] : 0.f;
   float dD_o = 0.f, dbias_o = 0.f;
 
@@ -207,8 +209,9 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     }
     cp_async_commit();
   };
-  // Register path: this thread's channel's own steps j = g + 4 i (delta, u, z, dy), one
-  // (step, state) element of B and C, and its states of the checkpoint.
+  // Register path: in the output mapping (channel lane, steps warp + 4 i) delta, u, z, dy; one
+  // (step, state) element of B and C; in the sweep mapping this lane's states of the
+  // checkpoint.
   float r_dl[STAGED ? 1 : kBT / kBG], r_u[STAGED ? 1 : kBT / kBG], r_z[STAGED ? 1 : kBT / kBG],
       r_dy[STAGED ? 1 : kBT / kBG], r_B[STAGED ? 1 : kBC], r_C[STAGED ? 1 : kBC],
       r_ck[STAGED ? 1 : kBK];
@@ -222,9 +225,9 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
       }
 #pragma unroll
       for (int i = 0; i < kBT / kBG; ++i) {
-        const int64_t t = t0 + g + kBG * i;
-        const bool tv = live && t < a.L;
-        const int64_t idx = (b * a.L + t) * a.dim + d;
+        const int64_t t = t0 + warp + (kBThreads / 32) * i;
+        const bool tv = live_o && t < a.L;
+        const int64_t idx = (b * a.L + t) * a.dim + d_o;
         r_dl[i] = tv ? to_f32(dl[idx]) : 0.f;
         r_u[i] = tv ? to_f32(u[idx]) : 0.f;
         r_z[i] = (tv && zz) ? to_f32(zz[idx]) : 0.f;
@@ -252,33 +255,35 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     const int64_t t0 = int64_t(ch) * kBT;
     // The chunk's per-(step, channel) values: dt, u, ds = dy SiLU(z), sigmoid(x) (softplus
     // slope), dy, SiLU'(z); steps past the end get dt = 0 and dy = 0 (an identity step).
+    // Output mapping: lane = channel, so a warp's accesses to a step row are contiguous.
+    static_assert(kBT % (kBThreads / 32) == 0 && kBCh == 32, "output mapping");
     float ck0[kBK];
 #pragma unroll
     for (int i = 0; i < kBT / kBG; ++i) {
-      const int j = g + kBG * i;
-      const bool tv = live && t0 + j < a.L;
+      const int j = warp + (kBThreads / 32) * i;
+      const bool tv = live_o && t0 + j < a.L;
       float xd, xu, xz, xy;
       if constexpr (STAGED) {
-        xd = to_f32(st_io[(0 * kBT + j) * kBCh + cl]);
-        xu = to_f32(st_io[(1 * kBT + j) * kBCh + cl]);
-        xz = zz ? to_f32(st_io[(2 * kBT + j) * kBCh + cl]) : 0.f;
-        xy = to_f32(st_io[(3 * kBT + j) * kBCh + cl]);
+        xd = to_f32(st_io[(0 * kBT + j) * kBCh + lane]);
+        xu = to_f32(st_io[(1 * kBT + j) * kBCh + lane]);
+        xz = zz ? to_f32(st_io[(2 * kBT + j) * kBCh + lane]) : 0.f;
+        xy = to_f32(st_io[(3 * kBT + j) * kBCh + lane]);
       } else {
         xd = r_dl[i];
         xu = r_u[i];
         xz = r_z[i];
         xy = r_dy[i];
       }
-      const float x = xd + bias;
+      const float x = xd + bias_o;
       float gz = 1.f, gp = 0.f;
       if (zz) {
         const float sg = sigmoid_f(xz);
         gz = xz * sg;
         gp = sg * fmaf(xz, 1.f - sg, 1.f);
       }
-      PA[j * kBCh + cl] = make_float4(tv ? (a.softplus ? softplus_f(x) : x) : 0.f, xu, xy * gz,
-                                      a.softplus ? sigmoid_f(x) : 1.f);
-      PB[j * kBCh + cl] = make_float2(xy, gp);
+      PA[j * kBCh + lane] = make_float4(tv ? (a.softplus ? softplus_f(x) : x) : 0.f, xu, xy * gz,
+                                        a.softplus ? sigmoid_f(x) : 1.f);
+      PB[j * kBCh + lane] = make_float2(xy, gp);
     }
 #pragma unroll
     for (int e = 0; e < kBC; ++e) {
@@ -292,13 +297,16 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
         Cs[idx] = r_C[e];
       }
     }
+    if constexpr (STAGED) {  // N is a multiple of 4 here: a lane's four states, or none
+      const float4 v = g * kBK < N ? *reinterpret_cast<const float4*>(st_ck + cl * N + g * kBK)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      ck0[0] = v.x;
+      ck0[1] = v.y;
+      ck0[2] = v.z;
+      ck0[3] = v.w;
+    } else {
 #pragma unroll
-    for (int k = 0; k < kBK; ++k) {
-      const int n = g * kBK + k;
-      if constexpr (STAGED)
-        ck0[k] = n < N ? st_ck[cl * N + n] : 0.f;
-      else
-        ck0[k] = r_ck[k];
+      for (int k = 0; k < kBK; ++k) ck0[k] = r_ck[k];
     }
     __syncthreads();  // table complete; the staging area is free
     if (ch > 0) prefetch(ch - 1);  // the next chunk's inputs, overlapping this chunk's work
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
           vB[k] = lam * dtu;
           vC[k] = ds * hist[jj + 1][k];
         }
-        R2[(j * kBCh + cl) * kBG + g] = make_float2(fmaf(uu, s1, s2), dt * s1);
+        R2[(j * kBG + g) * kBCh + (cl ^ ((g & 1) << 3))] = make_float2(fmaf(uu, s1, s2), dt * s1);
         // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
         // reduction: each round halves the values a lane keeps, so after three rounds lane
         // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
@@ -420,9 +428,13 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
     for (int i = 0; i < kBT / (kBThreads / 32); ++i) {
       const int j = warp + (kBThreads / 32) * i;
       const int64_t t = t0 + j;
-      const float4* r4 = reinterpret_cast<const float4*>(R2 + (j * kBCh + lane) * kBG);
-      const float4 ra = r4[0], rb = r4[1];  // {d(dt), du} of lanes 0, 1 and 2, 3
-      const float ddt = ((ra.x + ra.z) + rb.x) + rb.z, dup = ((ra.y + ra.w) + rb.y) + rb.w;
+      float ddt = 0.f, dup = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < kBG; ++gg) {
+        const float2 r = R2[(j * kBG + gg) * kBCh + (lane ^ ((gg & 1) << 3))];
+        ddt += r.x;
+        dup += r.y;
+      }
       const float sp = R1[j * kBCh + lane];
       const float4 q = PA[j * kBCh + lane];
       const float2 qb = PB[j * kBCh + lane];
