@@ -10,16 +10,20 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kHostStreams = 3;      // host path: streams the batch slices rotate over
+constexpr int64_t kHostSlices = 8;   // host path: at most this many batch slices per call
 
 struct DeviceState {
   unsigned int* status = nullptr;  // device status word
-  // host-path staging (device side), grown on demand
+  // host-path staging (device side), grown on demand, and the streams its slices run on
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  cudaStream_t host_streams[kHostStreams] = {};
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::mutex g_host_mu[kMaxDevices];  // one host-path call per device at a time
 
 int current_device() {
   int d = -1;
@@ -332,6 +336,7 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
   if (dev < 0) return SSCAN_ERR_CUDA;
   if (batch == 0 || dim == 0) return SSCAN_OK;
   const size_t es = dtype == SSCAN_F32 ? 4 : 2;
+  std::lock_guard<std::mutex> call_lock(g_host_mu[dev]);
   // Device staging layout, each piece 256-byte aligned.
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t s_bld = up(size_t(bld) * es), s_bln = up(size_t(bln) * es);
@@ -339,12 +344,13 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
   const size_t s_h = up(size_t(batch * dim * N) * 4);
   const size_t total = (3 + (z ? 1 : 0)) * s_bld + 2 * s_bln + s_A + 2 * s_dim + s_h;
   unsigned char* base = nullptr;
+  cudaStream_t hs[kHostStreams];
   {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState& ds = g_dev[dev];
     if (ds.stage_bytes < total) {
       if (ds.stage) {
-        cudaStreamSynchronize(stream);
+        cudaDeviceSynchronize();
         cudaFree(ds.stage);
       }
       ds.stage = nullptr;
@@ -352,38 +358,81 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
       if (cudaMalloc(&ds.stage, total) != cudaSuccess) return SSCAN_ERR_CUDA;
       ds.stage_bytes = total;
     }
+    for (int k = 0; k < kHostStreams; ++k) {
+      if (!ds.host_streams[k] &&
+          cudaStreamCreateWithFlags(&ds.host_streams[k], cudaStreamNonBlocking) != cudaSuccess) {
+        ds.host_streams[k] = nullptr;
+        return SSCAN_ERR_CUDA;
+      }
+      hs[k] = ds.host_streams[k];
+    }
     base = static_cast<unsigned char*>(ds.stage);
   }
   unsigned char* p = base;
   auto take = [&](size_t n) { unsigned char* r = p; p += n; return r; };
-  void* du = take(s_bld);
-  void* ddl = take(s_bld);
-  void* dy = take(s_bld);
-  void* dz = z ? take(s_bld) : nullptr;
-  void* dB = take(s_bln);
-  void* dC = take(s_bln);
+  unsigned char* du = take(s_bld);
+  unsigned char* ddl = take(s_bld);
+  unsigned char* dy = take(s_bld);
+  unsigned char* dz = z ? take(s_bld) : nullptr;
+  unsigned char* dB = take(s_bln);
+  unsigned char* dC = take(s_bln);
   float* dA = reinterpret_cast<float*>(take(s_A));
   float* dD = D ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
   float* dbias = delta_bias ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
   float* dh = h_last ? reinterpret_cast<float*>(take(s_h)) : nullptr;
-  auto h2d = [&](void* dst, const void* src, size_t n) {
-    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  auto copy = [](void* dst, const void* src, size_t n, cudaMemcpyKind kind, cudaStream_t s) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, kind, s) == cudaSuccess;
   };
-  const size_t nb = size_t(bld) * es, nbc = size_t(bln) * es;
-  bool ok = h2d(du, u, nb) && h2d(ddl, delta, nb) && (!z || h2d(dz, z, nb)) &&
-            h2d(dB, B, nbc) && h2d(dC, C, nbc) && h2d(dA, A, size_t(dim * N) * 4) &&
-            (!D || h2d(dD, D, size_t(dim) * 4)) &&
-            (!delta_bias || h2d(dbias, delta_bias, size_t(dim) * 4));
-  if (!ok) return SSCAN_ERR_CUDA;
-  st = sscan_fwd(du, ddl, dA, dB, dC, dD, dz, dbias, softplus_flag, dy, dh, batch, L, dim, N,
-                 dtype, stream);
-  if (st != SSCAN_OK) return st;
-  if (nb && cudaMemcpyAsync(y, dy, nb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return SSCAN_ERR_CUDA;
-  if (h_last && cudaMemcpyAsync(h_last, dh, size_t(batch * dim * N) * 4, cudaMemcpyDeviceToHost,
-                                stream) != cudaSuccess)
-    return SSCAN_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return SSCAN_ERR_CUDA;
+  const auto H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+  // Per-channel parameters on the caller's stream; then the batch is cut into slices that
+  // rotate over the library's streams, so one slice's host-to-device copy, another's scan and
+  // a third's device-to-host copy run at the same time.
+  bool ok = copy(dA, A, size_t(dim * N) * 4, H2D, stream) &&
+            (!D || copy(dD, D, size_t(dim) * 4, H2D, stream)) &&
+            (!delta_bias || copy(dbias, delta_bias, size_t(dim) * 4, H2D, stream));
+  cudaEvent_t ev_start = nullptr, ev_done[kHostStreams] = {};
+  ok = ok && cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
+  for (int k = 0; k < kHostStreams && ok; ++k)
+    ok = cudaEventCreateWithFlags(&ev_done[k], cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventRecord(ev_start, stream) == cudaSuccess;
+  for (int k = 0; k < kHostStreams && ok; ++k)
+    ok = cudaStreamWaitEvent(hs[k], ev_start, 0) == cudaSuccess;
+  const int64_t n_slices = batch < kHostSlices ? batch : kHostSlices;
+  const int64_t rows = (batch + n_slices - 1) / n_slices;
+  const unsigned char* hu = static_cast<const unsigned char*>(u);
+  const unsigned char* hdl = static_cast<const unsigned char*>(delta);
+  const unsigned char* hz = static_cast<const unsigned char*>(z);
+  const unsigned char* hB = static_cast<const unsigned char*>(B);
+  const unsigned char* hC = static_cast<const unsigned char*>(C);
+  unsigned char* hy = static_cast<unsigned char*>(y);
+  for (int64_t r0 = 0, i = 0; r0 < batch && ok; r0 += rows, ++i) {
+    const int64_t nr = batch - r0 < rows ? batch - r0 : rows;
+    cudaStream_t s = hs[i % kHostStreams];
+    const size_t o = size_t(r0 * L * dim) * es, n = size_t(nr * L * dim) * es;
+    const size_t ob = size_t(r0 * L * N) * es, nbc = size_t(nr * L * N) * es;
+    ok = copy(du + o, hu + o, n, H2D, s) && copy(ddl + o, hdl + o, n, H2D, s) &&
+         (!z || copy(dz + o, hz + o, n, H2D, s)) && copy(dB + ob, hB + ob, nbc, H2D, s) &&
+         copy(dC + ob, hC + ob, nbc, H2D, s);
+    float* dhs = dh ? dh + r0 * dim * N : nullptr;
+    if (ok) {
+      st = sscan_fwd(du + o, ddl + o, dA, dB + ob, dC + ob, dD, z ? dz + o : nullptr, dbias,
+                     softplus_flag, dy + o, dhs, nr, L, dim, N, dtype, s);
+      ok = st == SSCAN_OK;
+    }
+    ok = ok && copy(hy + o, dy + o, n, D2H, s) &&
+         (!h_last || copy(h_last + r0 * dim * N, dhs, size_t(nr * dim * N) * 4, D2H, s));
+  }
+  for (int k = 0; k < kHostStreams; ++k) {
+    if (ok) ok = cudaEventRecord(ev_done[k], hs[k]) == cudaSuccess &&
+                 cudaStreamWaitEvent(stream, ev_done[k], 0) == cudaSuccess;
+  }
+  if (ok) ok = cudaStreamSynchronize(stream) == cudaSuccess;
+  if (!ok)  // nothing may still be reading or writing the caller's buffers when this returns
+    for (int k = 0; k < kHostStreams; ++k) cudaStreamSynchronize(hs[k]);
+  if (ev_start) cudaEventDestroy(ev_start);
+  for (int k = 0; k < kHostStreams; ++k)
+    if (ev_done[k]) cudaEventDestroy(ev_done[k]);
+  if (!ok) return st != SSCAN_OK ? st : SSCAN_ERR_CUDA;
   return SSCAN_OK;
 }
 
@@ -415,7 +464,9 @@ sscan_status_t sscan_release(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& s = g_dev[dev];
   cudaError_t e = cudaSuccess;
-  if (s.status) e = cudaFree(s.status);
+  for (int k = 0; k < kHostStreams; ++k)
+    if (s.host_streams[k] && e == cudaSuccess) e = cudaStreamDestroy(s.host_streams[k]);
+  if (s.status && e == cudaSuccess) e = cudaFree(s.status);
   if (s.stage && e == cudaSuccess) e = cudaFree(s.stage);
   s = DeviceState();
   return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;

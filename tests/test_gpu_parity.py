@@ -184,14 +184,36 @@ def test_bitwise_deterministic():
     assert torch.equal(y1, y2) and torch.equal(h1, h2)
 
 
+def _rows(x, r0, r1):
+    return {k: (v[r0:r1].contiguous() if v is not None and v.dim() == 3 and k != "A" else v)
+            for k, v in x.items()}
+
+
 def test_host_entry_matches_device_entry():
+    """The host entry cuts a batch of up to 8 rows into one-row slices: each equals the device
+    entry run on that row alone."""
     w = WORKLOADS["fp32"].replace(batch=2, L=200, dim=128)
     x = make_inputs(w, device=DEV)
-    y, h = run_lib(x)
     xc = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
     yh, hh = binding.fwd_host(xc["u"], xc["delta"], xc["A"], xc["B"], xc["C"], xc["D"], xc["z"],
                               xc["delta_bias"])
-    assert torch.equal(yh, y.cpu()) and torch.equal(hh, h.cpu())
+    for r in range(w.batch):
+        y, h = run_lib(_rows(x, r, r + 1))
+        assert torch.equal(yh[r:r + 1], y.cpu()) and torch.equal(hh[r:r + 1], h.cpu()), r
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_host_entry_many_slices(io):
+    """19 batch rows: slices of 3 rows rotating over the library's streams, against the
+    oracle."""
+    base = WORKLOADS["fp32"] if io == "f32" else WORKLOADS["bf16"]
+    w = base.replace(batch=19, L=150, dim=64)
+    x = make_inputs(w, device=DEV)
+    xc = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+    yh, hh = binding.fwd_host(xc["u"], xc["delta"], xc["A"], xc["B"], xc["C"], xc["D"], xc["z"],
+                              xc["delta_bias"])
+    yr, hr = oracle_full(x)
+    assert_within(compare(yh, hh, yr, hr, w.io), w.io, f"host entry, 19 rows, {io}")
 
 
 def test_invalid_arguments_rejected_synchronously():
