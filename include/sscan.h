@@ -172,11 +172,15 @@ sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bia
 
 /*
  * sscan_fwd_host -- the same operation on HOST buffers: copies the inputs to the current
- * device on `stream`, runs sscan_fwd, copies y and h_last back and synchronizes `stream`.
+ * device, runs sscan_fwd, copies y and h_last back and synchronizes `stream`.
  * Arguments mean what they mean for sscan_fwd but every pointer is host memory (page-locked
- * memory gives asynchronous, overlapped copies). Device staging buffers are owned by the library
- * per device, grown on demand and kept until sscan_release(). Returns when y and h_last hold the
- * result, or with the first error.
+ * memory gives asynchronous, overlapped copies). The batch is cut into up to 8 slices of whole
+ * batch rows that rotate over three streams the library owns (ordered after the work already
+ * on `stream`; `stream` waits for all of them), so one slice's copy in, another's scan and a
+ * third's copy out overlap; each slice is an independent sscan_fwd over its rows. Device staging
+ * buffers and those streams are owned by the library per device, grown or created on demand and
+ * kept until sscan_release(). Calls on one device are serialised inside the library. Returns when
+ * y and h_last hold the result, or with the first error (after every copy it queued has ended).
  */
 sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
                               const void* C, const float* D, const void* z,
