@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "sscan_device.cuh"
 #include "sscan_internal.h"
@@ -35,6 +36,8 @@ namespace {
 
 constexpr int kBT = 16;      // steps per chunk
 constexpr int kBH = kBT / 2; // steps per half-chunk sweep
+constexpr int kMinSegChunks = 8;
+constexpr float kLn2 = 0.6931471805599453f;  // 1 / log2(e)  // shortest time segment of the backward, in chunks
 constexpr int kBG = 4;       // lanes per channel
 constexpr int kBK = 4;       // states per lane (N <= 16)
 constexpr int kBThreads = 128;  // three blocks per SM under the 170-register budget
@@ -90,13 +93,26 @@ struct BwdSmem {
   }
 };
 
+// Time segments of a (batch row, channel group) tile. With n_seg > 1 a first launch
+// (agg_mode) runs the adjoint recurrence alone over each segment but the first, from zero at
+// the segment's end, and records per lane the adjoint at the segment's start (mu_local) and the
+// segment's decay (sum of dt for zero-order hold, product of factors for first order); the
+// second launch starts every segment from dh_last folded back through the aggregates of all
+// later segments, nearest last, in a fixed order.
+struct BwdSeg {
+  int n_seg = 1;       // segments per tile
+  int seg_chunks = 0;  // chunks per segment
+  float* agg = nullptr;  // [n_seg][batch][n_groups][kBThreads][kAggF]
+};
+constexpr int kAggF = 8;  // mu_local[4], then sum dt (zero-order hold) or products[4]
+
 // STAGED: the next chunk's inputs are copied into shared memory with cp.async while the current
 // one is processed (needs dim and N rows in whole 16-byte pieces and 16-byte aligned tensors);
 // otherwise each thread loads them into registers a chunk ahead. MINB: resident CTAs per SM the
-// register budget is cut for.
-template <typename IO, bool EULER, bool STAGED, int MINB>
+// register budget is cut for. AGG: the aggregate launch of a time-segmented backward.
+template <typename IO, bool EULER, bool STAGED, int MINB, bool AGG = false>
 __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, int n_chunks,
-                                                                    int n_groups,
+                                                                    int n_groups, BwdSeg sg,
                                                                     unsigned* __restrict__ tiles,
                                                                     float* __restrict__ part_dB,
                                                                     float* __restrict__ part_dC,
@@ -137,33 +153,53 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
   const size_t part_stride = size_t(a.batch) * a.L * 16;  // one channel group's [b][t][16]
   constexpr int kBC = kBT * 16 / kBThreads;  // B / C elements per thread and chunk
 
-  // Persistent blocks: each takes (batch row, channel group) tiles from a counter until none
-  // are left, so the last wave does not leave SMs idle.
+  // Persistent blocks: each takes (segment, batch row, channel group) units from a counter until
+  // none are left, so the last wave does not leave SMs idle. The aggregate launch covers
+  // segments 1 .. n_seg - 1.
   __shared__ unsigned s_tile;
-  const unsigned n_tiles = unsigned(a.batch) * unsigned(n_groups);
+  const unsigned per_seg = unsigned(a.batch) * unsigned(n_groups);
+  const unsigned n_units = per_seg * unsigned(AGG ? sg.n_seg - 1 : sg.n_seg);
   for (;;) {
   if (tid == 0) s_tile = atomicAdd(tiles, 1u);
   __syncthreads();
-  const unsigned tile = s_tile;
-  __syncthreads();  // every thread has read the tile before thread 0 fetches the next
-  if (tile >= n_tiles) break;
+  const unsigned unit = s_tile;
+  __syncthreads();  // every thread has read the unit before thread 0 fetches the next
+  if (unit >= n_units) break;
+  const int seg = int(unit / per_seg) + (AGG ? 1 : 0);
+  const unsigned tile = unit % per_seg;
   const int64_t b = tile / unsigned(n_groups);
   const int cg_idx = int(tile % unsigned(n_groups));
+  const int c_lo = seg * sg.seg_chunks;
+  const int c_hi = min(n_chunks, c_lo + sg.seg_chunks) - 1;
+  const size_t seg_row = size_t(seg) * a.batch + b;  // row of this unit's dA, dD, dbias partials
   const int64_t ch0 = int64_t(cg_idx) * kBCh;
   const int64_t d = ch0 + cl;
   const bool live = d < a.dim;
   const int64_t c = b * a.dim + d;
   const int64_t d_o = ch0 + lane;  // output mapping's channel
   const bool live_o = d_o < a.dim;
-  float a2[kBK], Av[kBK], mu[kBK], dA[kBK];
+  float a2[kBK], mu[kBK], dA[kBK];  // a2 = A log2e (zero-order hold) or A (first order)
 #pragma unroll
   for (int k = 0; k < kBK; ++k) {
     const int n = g * kBK + k;
-    Av[k] = (live && n < N) ? a.A[d * N + n] : 0.f;
-    a2[k] = Av[k] * (EULER ? 1.f : kLog2e);
-    mu[k] = (live && a.dh_last && n < N) ? a.dh_last[c * N + n] : 0.f;
+    a2[k] = ((live && n < N) ? a.A[d * N + n] : 0.f) * (EULER ? 1.f : kLog2e);
+    mu[k] = (!AGG && live && a.dh_last && n < N) ? a.dh_last[c * N + n] : 0.f;
     dA[k] = 0.f;
   }
+  // The adjoint entering this segment from the right: dh_last carried back through every later
+  // segment (mu <- decay_j mu + mu_local_j, from the last segment down).
+  if (!AGG) {
+    for (int j = sg.n_seg - 1; j > seg; --j) {
+      const float* ag = sg.agg + ((size_t(j) * a.batch + b) * n_groups + cg_idx) * kBThreads * kAggF +
+                        size_t(tid) * kAggF;
+#pragma unroll
+      for (int k = 0; k < kBK; ++k) {
+        const float P = EULER ? ag[4 + k] : ex2(a2[k] * ag[4]);
+        mu[k] = fmaf(P, mu[k], ag[k]);
+      }
+    }
+  }
+  float sdt = 0.f, Pr[kBK] = {1.f, 1.f, 1.f, 1.f};  // aggregate launch: the segment's decay
   const float bias_o = (live_o && a.bias) ? a.bias[d_o] : 0.f;
   const float D_o = (live_o && a.D) ? a.D[d_o] : 0.f;
   float dD_o = 0.f, dbias_o = 0.f;
@@ -245,13 +281,13 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
       issue_stage(ch);
     }
   };
-  prefetch(n_chunks - 1);
+  prefetch(c_hi);
   if constexpr (STAGED) {
     cp_async_wait_all();
     __syncthreads();
   }
 
-  for (int ch = n_chunks - 1; ch >= 0; --ch) {
+  for (int ch = c_hi; ch >= c_lo; --ch) {
     const int64_t t0 = int64_t(ch) * kBT;
     // The chunk's per-(step, channel) values: dt, u, ds = dy SiLU(z), sigmoid(x) (softplus
     // slope), dy, SiLU'(z); steps past the end get dt = 0 and dy = 0 (an identity step).
@@ -309,156 +345,187 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
       for (int k = 0; k < kBK; ++k) ck0[k] = r_ck[k];
     }
     __syncthreads();  // table complete; the staging area is free
-    if (ch > 0) prefetch(ch - 1);  // the next chunk's inputs, overlapping this chunk's work
+    if (ch > c_lo) prefetch(ch - 1);  // the next chunk's inputs, overlapping this chunk's work
 
-    // Recompute and sweep the chunk in two halves (steps kBH .. kBT - 1, then 0 .. kBH - 1), each
-    // recomputing its states from the checkpoint: a lane keeps kBH + 1 states per slot instead
-    // of kBT + 1, which leaves registers for more resident warps. hist[jj] is the state before
-    // step t0 + j0 + jj.
-    float* wB = sdB + size_t(warp) * kBT * 16;
-    float* wC = sdC + size_t(warp) * kBT * 16;
+    if constexpr (AGG) {
+      // The adjoint recurrence alone, from zero at the segment's end; and the segment's decay.
+      float csum = 0.f;
 #pragma unroll
-    for (int half = 1; half >= 0; --half) {
-      const int j0 = half * kBH;
-      float hist[kBH + 1][kBK];
-#pragma unroll
-      for (int k = 0; k < kBK; ++k) hist[0][k] = ck0[k];
-#pragma unroll
-      for (int j = 0; j < j0; ++j) {  // advance to step j0 (its readout part is the other half's)
-        const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
-        const float dt = q.x, dtu = dt * q.y;
-        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
-        const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-        for (int k = 0; k < kBK; ++k)
-          hist[0][k] = fmaf(factor<EULER>(dt, a2[k]), hist[0][k], dtu * bv[k]);
-      }
-#pragma unroll
-      for (int jj = 0; jj < kBH; ++jj) {
-        const int j = j0 + jj;
-        const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
-        const float dt = q.x, dtu = dt * q.y;
-        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
-        const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
-        const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
-        float sp = 0.f;
-#pragma unroll
-        for (int k = 0; k < kBK; ++k) {
-          hist[jj + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[jj][k], dtu * bv[k]);
-          sp = fmaf(cv[k], hist[jj + 1][k], sp);
-        }
-        // The readout's state part summed over the channel's four lanes (all four store it).
-        sp += __shfl_xor_sync(0xffffffffu, sp, 1);
-        sp += __shfl_xor_sync(0xffffffffu, sp, 2);
-        R1[j * kBCh + cl] = sp;
-      }
-      // Adjoint sweep back through the half. No branches and no global stores: the steps of the
-      // unrolled loop overlap, tied only by the lam / mu recurrence.
-#pragma unroll
-      for (int jj = kBH - 1; jj >= 0; --jj) {
-        const int j = j0 + jj;
+      for (int j = kBT - 1; j >= 0; --j) {
         const float4 q = PA[j * kBCh + cl];
-        const float dt = q.x, uu = q.y, ds = q.z, dtu = dt * uu;
-        const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
         const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
-        const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
-        // s1 = sum_n lam B (gives d(dt) through the input term, u s1, and du, dt s1);
-        // s2 = sum_n A lam h_{t-1} da/d(dt) / A (the decay term of d(dt)).
-        float s1 = 0.f, s2 = 0.f, vB[kBK], vC[kBK];
+        const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
+        csum += q.x;
 #pragma unroll
         for (int k = 0; k < kBK; ++k) {
-          const float fa = factor<EULER>(dt, a2[k]);
-          const float lam = fmaf(ds, cv[k], mu[k]);
-          mu[k] = fa * lam;
-          // lam h_{t-1} times da/d(dt) / A: a (zero-order hold) or 1 (first order); times dt
-          // it is the dA term.
-          const float dfa = (EULER ? lam : mu[k]) * hist[jj][k];
-          s2 = fmaf(dfa, Av[k], s2);
-          dA[k] = fmaf(dfa, dt, dA[k]);
-          s1 = fmaf(lam, bv[k], s1);
-          vB[k] = lam * dtu;
-          vC[k] = ds * hist[jj + 1][k];
+          const float fa = factor<EULER>(q.x, a2[k]);
+          mu[k] = fa * fmaf(q.z, cv[k], mu[k]);
+          if constexpr (EULER) Pr[k] *= fa;
         }
-        R2[(j * kBG + g) * kBCh + (cl ^ ((g & 1) << 3))] = make_float2(fmaf(uu, s1, s2), dt * s1);
-        // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
-        // reduction: each round halves the values a lane keeps, so after three rounds lane
-        // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
-        // {dB[0..3], dC[0..3]}, and writes it to the warp's slot.
-        {
-          const bool b0 = (lane & 4) != 0, b1 = (lane & 8) != 0, b2 = (lane & 16) != 0;
-          float r1[4], r2[2];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float keep = b0 ? vC[i] : vB[i], send = b0 ? vB[i] : vC[i];
-            r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      sdt += csum;
+    } else {
+
+      // Recompute and sweep the chunk in two halves (steps kBH .. kBT - 1, then 0 .. kBH - 1), each
+      // recomputing its states from the checkpoint: a lane keeps kBH + 1 states per slot instead
+      // of kBT + 1, which leaves registers for more resident warps. hist[jj] is the state before
+      // step t0 + j0 + jj.
+      float* wB = sdB + size_t(warp) * kBT * 16;
+      float* wC = sdC + size_t(warp) * kBT * 16;
+  #pragma unroll
+      for (int half = 1; half >= 0; --half) {
+        const int j0 = half * kBH;
+        float hist[kBH + 1][kBK];
+  #pragma unroll
+        for (int k = 0; k < kBK; ++k) hist[0][k] = ck0[k];
+  #pragma unroll
+        for (int j = 0; j < j0; ++j) {  // advance to step j0 (its readout part is the other half's)
+          const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
+          const float dt = q.x, dtu = dt * q.y;
+          const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+          const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+  #pragma unroll
+          for (int k = 0; k < kBK; ++k)
+            hist[0][k] = fmaf(factor<EULER>(dt, a2[k]), hist[0][k], dtu * bv[k]);
+        }
+  #pragma unroll
+        for (int jj = 0; jj < kBH; ++jj) {
+          const int j = j0 + jj;
+          const float2 q = *reinterpret_cast<const float2*>(PA + j * kBCh + cl);  // dt, u
+          const float dt = q.x, dtu = dt * q.y;
+          const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+          const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+          const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
+          float sp = 0.f;
+  #pragma unroll
+          for (int k = 0; k < kBK; ++k) {
+            hist[jj + 1][k] = fmaf(factor<EULER>(dt, a2[k]), hist[jj][k], dtu * bv[k]);
+            sp = fmaf(cv[k], hist[jj + 1][k], sp);
           }
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float keep = b1 ? r1[2 + i] : r1[i], send = b1 ? r1[i] : r1[2 + i];
-            r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          // The readout's state part summed over the channel's four lanes (all four store it).
+          sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+          sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+          R1[j * kBCh + cl] = sp;
+        }
+        // Adjoint sweep back through the half. No branches and no global stores: the steps of the
+        // unrolled loop overlap, tied only by the lam / mu recurrence.
+  #pragma unroll
+        for (int jj = kBH - 1; jj >= 0; --jj) {
+          const int j = j0 + jj;
+          const float4 q = PA[j * kBCh + cl];
+          const float dt = q.x, uu = q.y, ds = q.z, dtu = dt * uu;
+          const float4 bq = *reinterpret_cast<const float4*>(Bs + j * 16 + g * kBK);
+          const float4 cq = *reinterpret_cast<const float4*>(Cs + j * 16 + g * kBK);
+          const float bv[4] = {bq.x, bq.y, bq.z, bq.w}, cv[4] = {cq.x, cq.y, cq.z, cq.w};
+          // s1 = sum_n lam B (gives d(dt) through the input term, u s1, and du, dt s1);
+          // s2 = sum_n A lam h_{t-1} da/d(dt) / A (the decay term of d(dt)).
+          float s1 = 0.f, s2 = 0.f, vB[kBK], vC[kBK];
+  #pragma unroll
+          for (int k = 0; k < kBK; ++k) {
+            const float fa = factor<EULER>(dt, a2[k]);
+            const float lam = fmaf(ds, cv[k], mu[k]);
+            mu[k] = fa * lam;
+            // lam h_{t-1} times da/d(dt) / A: a (zero-order hold) or 1 (first order); times dt
+            // it is the dA term.
+            const float dfa = (EULER ? lam : mu[k]) * hist[jj][k];
+            s2 = fmaf(dfa, a2[k], s2);  // A scaled as a2; rescaled below
+            dA[k] = fmaf(dfa, dt, dA[k]);
+            s1 = fmaf(lam, bv[k], s1);
+            vB[k] = lam * dtu;
+            vC[k] = ds * hist[jj + 1][k];
           }
-          const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
-          const float r3 = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-          (b0 ? wC : wB)[j * 16 + g * kBK + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = r3;
+          R2[(j * kBG + g) * kBCh + (cl ^ ((g & 1) << 3))] =
+              make_float2(fmaf(uu, s1, EULER ? s2 : s2 * kLn2), dt * s1);
+          // dB, dC: sum over the warp's 8 channels (lanes with the same g) by a transposing
+          // reduction: each round halves the values a lane keeps, so after three rounds lane
+          // (channel bits b0 b1 b2) holds the full sum of value q = 4 b0 + 2 b1 + b2 of
+          // {dB[0..3], dC[0..3]}, and writes it to the warp's slot.
+          {
+            const bool b0 = (lane & 4) != 0, b1 = (lane & 8) != 0, b2 = (lane & 16) != 0;
+            float r1[4], r2[2];
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float keep = b0 ? vC[i] : vB[i], send = b0 ? vB[i] : vC[i];
+              r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+  #pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float keep = b1 ? r1[2 + i] : r1[i], send = b1 ? r1[i] : r1[2 + i];
+              r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+            const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
+            const float r3 = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            (b0 ? wC : wB)[j * 16 + g * kBK + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = r3;
+          }
         }
       }
-    }
-    __syncthreads();
-    // The CTA's partial of this chunk (warp slots added in order) to its channel group's slice.
-#pragma unroll
-    for (int e = 0; e < kBC; ++e) {
-      const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
-      const int64_t t = t0 + j;
-      if (t < a.L && n < N) {
-        float sb = 0.f, sc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kBThreads / 32; ++w) {
-          sb += sdB[(size_t(w) * kBT + j) * 16 + n];
-          sc += sdC[(size_t(w) * kBT + j) * 16 + n];
+      __syncthreads();
+      // The CTA's partial of this chunk (warp slots added in order) to its channel group's slice.
+  #pragma unroll
+      for (int e = 0; e < kBC; ++e) {
+        const int idx = tid + e * kBThreads, j = idx / 16, n = idx % 16;
+        const int64_t t = t0 + j;
+        if (t < a.L && n < N) {
+          float sb = 0.f, sc = 0.f;
+  #pragma unroll
+          for (int w = 0; w < kBThreads / 32; ++w) {
+            sb += sdB[(size_t(w) * kBT + j) * 16 + n];
+            sc += sdC[(size_t(w) * kBT + j) * 16 + n];
+          }
+          const size_t o = size_t(cg_idx) * part_stride + (size_t(b) * a.L + t) * 16 + n;
+          part_dB[o] = sb;
+          part_dC[o] = sc;
         }
-        const size_t o = size_t(cg_idx) * part_stride + (size_t(b) * a.L + t) * 16 + n;
-        part_dB[o] = sb;
-        part_dC[o] = sc;
       }
-    }
-    // Per-(step, channel) outputs: the four lanes' partials summed in lane order, then
-    // ddelta = d(dt) sigmoid(x), du = ds D + sum_n lam dt B, dz = dy (D u + readout) SiLU'(z).
-    // A warp's store covers 32 consecutive channels of one step.
-#pragma unroll
-    for (int i = 0; i < kBT / (kBThreads / 32); ++i) {
-      const int j = warp + (kBThreads / 32) * i;
-      const int64_t t = t0 + j;
-      float ddt = 0.f, dup = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < kBG; ++gg) {
-        const float2 r = R2[(j * kBG + gg) * kBCh + (lane ^ ((gg & 1) << 3))];
-        ddt += r.x;
-        dup += r.y;
-      }
-      const float sp = R1[j * kBCh + lane];
-      const float4 q = PA[j * kBCh + lane];
-      const float2 qb = PB[j * kBCh + lane];
-      if (live_o && t < a.L) {
-        const int64_t o = (b * a.L + t) * a.dim + d_o;
-        const float dx = ddt * q.w;
-        store_io(static_cast<IO*>(a.du) + o, fmaf(q.z, D_o, dup));
-        store_io(static_cast<IO*>(a.ddelta) + o, dx);
-        if (zz) store_io(static_cast<IO*>(a.dz) + o, qb.x * fmaf(D_o, q.y, sp) * qb.y);
-        dbias_o += dx;
-        dD_o = fmaf(q.z, q.y, dD_o);
+      // Per-(step, channel) outputs: the four lanes' partials summed in lane order, then
+      // ddelta = d(dt) sigmoid(x), du = ds D + sum_n lam dt B, dz = dy (D u + readout) SiLU'(z).
+      // A warp's store covers 32 consecutive channels of one step.
+  #pragma unroll
+      for (int i = 0; i < kBT / (kBThreads / 32); ++i) {
+        const int j = warp + (kBThreads / 32) * i;
+        const int64_t t = t0 + j;
+        float ddt = 0.f, dup = 0.f;
+  #pragma unroll
+        for (int gg = 0; gg < kBG; ++gg) {
+          const float2 r = R2[(j * kBG + gg) * kBCh + (lane ^ ((gg & 1) << 3))];
+          ddt += r.x;
+          dup += r.y;
+        }
+        const float sp = R1[j * kBCh + lane];
+        const float4 q = PA[j * kBCh + lane];
+        const float2 qb = PB[j * kBCh + lane];
+        if (live_o && t < a.L) {
+          const int64_t o = (b * a.L + t) * a.dim + d_o;
+          const float dx = ddt * q.w;
+          store_io(static_cast<IO*>(a.du) + o, fmaf(q.z, D_o, dup));
+          store_io(static_cast<IO*>(a.ddelta) + o, dx);
+          if (zz) store_io(static_cast<IO*>(a.dz) + o, qb.x * fmaf(D_o, q.y, sp) * qb.y);
+          dbias_o += dx;
+          dD_o = fmaf(q.z, q.y, dD_o);
+        }
       }
     }
     if constexpr (STAGED) cp_async_wait_all();  // the next chunk's inputs have landed
     __syncthreads();  // table, partials and warp slots are reused; staged inputs are visible
   }
+  if constexpr (AGG) {
+    float* ag = sg.agg + ((size_t(seg) * a.batch + b) * n_groups + cg_idx) * kBThreads * kAggF +
+                size_t(tid) * kAggF;
+#pragma unroll
+    for (int k = 0; k < kBK; ++k) {
+      ag[k] = mu[k];
+      ag[4 + k] = EULER ? Pr[k] : (k == 0 ? sdt : 0.f);
+    }
+    continue;  // the unit loop's barriers order this before the next unit's shared-memory use
+  }
   if (live) {
-    // dh0 = a_0 lam_0; per-batch-row partials of dA.
+    // dh0 = a_0 lam_0 (first segment); per-(segment, batch row) partials of dA.
 #pragma unroll
     for (int k = 0; k < kBK; ++k) {
       const int n = g * kBK + k;
       if (n < N) {
-        if (a.dh0) a.dh0[c * N + n] = mu[k];
-        part_dA[(size_t(b) * a.dim + d) * N + n] = dA[k];
+        if (a.dh0 && seg == 0) a.dh0[c * N + n] = mu[k];
+        part_dA[(seg_row * a.dim + d) * N + n] = dA[k];
       }
     }
   }
@@ -473,14 +540,14 @@ __global__ void __launch_bounds__(kBThreads, MINB) bwd_chunk_kernel(BwdArgs a, i
       sD += v.x;
       sb += v.y;
     }
-    part_dD[size_t(b) * a.dim + d_o] = sD;
-    part_db[size_t(b) * a.dim + d_o] = sb;
+    part_dD[seg_row * a.dim + d_o] = sD;
+    part_db[seg_row * a.dim + d_o] = sb;
   }
   }  // tiles
 }
 
 // ---- 3. fixed-order sums of the partials -------------------------------------------------------
-__global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups,
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups, int n_seg,
                                                          const float* __restrict__ part_dB,
                                                          const float* __restrict__ part_dC,
                                                          const float* __restrict__ part_dA,
@@ -489,6 +556,7 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups
   const int64_t N = a.N;
   const int64_t nbc = a.batch * a.L * N, ndn = a.dim * N;
   const size_t part_stride = size_t(a.batch) * a.L * 16;
+  const int64_t rows = int64_t(n_seg) * a.batch;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nbc + ndn + 2 * a.dim;
        i += int64_t(gridDim.x) * blockDim.x) {
     if (i < nbc) {  // dB, dC over channel groups
@@ -500,12 +568,12 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups
       }
       a.dB[i] = sb;
       a.dC[i] = sc;
-    } else if (i < nbc + ndn) {  // dA over batch rows
+    } else if (i < nbc + ndn) {  // dA over (segment, batch row) rows
       const int64_t j = i - nbc;
       float s = 0.f;
-      for (int64_t b = 0; b < a.batch; ++b) s += part_dA[size_t(b) * ndn + j];
+      for (int64_t b = 0; b < rows; ++b) s += part_dA[size_t(b) * ndn + j];
       a.dA[j] = s;
-    } else {  // dD, dbias over batch rows
+    } else {  // dD, dbias over (segment, batch row) rows
       const int64_t j = i - nbc - ndn;
       const bool isD = j < a.dim;
       const int64_t dd = isD ? j : j - a.dim;
@@ -513,7 +581,7 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(BwdArgs a, int n_groups
       float* out = isD ? a.dD : a.dbias;
       if (!out) continue;
       float s = 0.f;
-      for (int64_t b = 0; b < a.batch; ++b) s += p[size_t(b) * a.dim + dd];
+      for (int64_t b = 0; b < rows; ++b) s += p[size_t(b) * a.dim + dd];
       out[dd] = s;
     }
   }
@@ -524,12 +592,32 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
   static_assert((kBT * 16) % kBThreads == 0, "whole B / C elements per thread and chunk");
   const int n_chunks = int((a.L + kBT - 1) / kBT);
   const int n_groups = int((a.dim + kBCh - 1) / kBCh);
+  int sms = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // Time segments only when there are fewer tiles than SMs (measured: with a tile per SM or
+  // more, the aggregate pass costs more than the added parallelism returns): then about two
+  // units per resident CTA, segments of at least kMinSegChunks chunks.
+  const int64_t n_tiles = int64_t(n_groups) * a.batch;
+  BwdSeg sg;
+  {
+    const int64_t resident = int64_t(3) * sms;
+    int64_t want = n_tiles >= sms ? 1 : (2 * resident + n_tiles - 1) / n_tiles;
+    want = std::min<int64_t>(want, std::max(1, n_chunks / kMinSegChunks));
+    if (const char* v = std::getenv("SSCAN_BWD_SEGMENTS")) want = std::max(1, std::atoi(v));
+    want = std::min<int64_t>(want, n_chunks);
+    sg.seg_chunks = int((n_chunks + want - 1) / want);
+    sg.n_seg = (n_chunks + sg.seg_chunks - 1) / sg.seg_chunks;
+  }
+  const int64_t n_units = n_tiles * sg.n_seg;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t pbc = up(size_t(n_groups) * a.batch * a.L * 16 * sizeof(float));
-  const size_t pa = up(size_t(a.batch) * a.dim * a.N * sizeof(float));
-  const size_t pd = up(size_t(a.batch) * a.dim * sizeof(float));
+  const size_t pa = up(size_t(sg.n_seg) * a.batch * a.dim * a.N * sizeof(float));
+  const size_t pd = up(size_t(sg.n_seg) * a.batch * a.dim * sizeof(float));
+  const size_t pg = sg.n_seg > 1 ? up(size_t(n_units) * kBThreads * kAggF * sizeof(float)) : 0;
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, 2 * pbc + pa + 2 * pd + 256, a.stream);
+  e = cudaMallocAsync(&ws, 2 * pbc + pa + 2 * pd + pg + 256, a.stream);
   if (e != cudaSuccess) return e;
   char* p = static_cast<char*>(ws);
   float* part_dB = reinterpret_cast<float*>(p);
@@ -537,20 +625,18 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
   float* part_dA = reinterpret_cast<float*>(p + 2 * pbc);
   float* part_dD = reinterpret_cast<float*>(p + 2 * pbc + pa);
   float* part_db = reinterpret_cast<float*>(p + 2 * pbc + pa + pd);
-  unsigned* tiles = reinterpret_cast<unsigned*>(p + 2 * pbc + pa + 2 * pd);
-  e = cudaMemsetAsync(tiles, 0, sizeof(unsigned), a.stream);
-  int sms = 0, dev = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sg.agg = pg ? reinterpret_cast<float*>(p + 2 * pbc + pa + 2 * pd) : nullptr;
+  unsigned* tiles = reinterpret_cast<unsigned*>(p + 2 * pbc + pa + 2 * pd + pg);  // 2 counters
+  e = cudaMemsetAsync(tiles, 0, 2 * sizeof(unsigned), a.stream);
   // Staged inputs need every copied row segment in whole, aligned 16-byte pieces.
   auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   const bool staged = (a.dim * int64_t(sizeof(IO))) % 16 == 0 &&
                       (a.N * int64_t(sizeof(IO))) % 16 == 0 && al(a.u) && al(a.delta) &&
                       al(a.dy) && al(a.B) && al(a.C) && (!a.z || al(a.z)) && al(a.ckpt);
-  // Four resident CTAs per SM (a tighter register budget) only when there are tiles for them.
-  const int64_t n_tiles = int64_t(n_groups) * a.batch;
-  const bool four = n_tiles > int64_t(3) * sms;
-  auto launch = [&](auto kern, bool st) -> cudaError_t {
+  // Four resident CTAs per SM (a tighter register budget) only when there are units for them.
+  const bool four = n_units > int64_t(3) * sms;
+  auto launch = [&](auto kern, bool st, const BwdSeg& s, unsigned* counter,
+                    int64_t units) -> cudaError_t {
     const size_t smem = BwdSmem<IO>::bytes(st);
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
@@ -559,24 +645,29 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
       r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBThreads, smem);
     if (r != cudaSuccess) return r;
     const unsigned grid = unsigned(std::max<int64_t>(
-        1, std::min<int64_t>(n_tiles, int64_t(std::max(per_sm, 1)) * sms)));
-    kern<<<grid, kBThreads, smem, a.stream>>>(a, n_chunks, n_groups, tiles, part_dB, part_dC,
-                                              part_dA, part_dD, part_db);
+        1, std::min<int64_t>(units, int64_t(std::max(per_sm, 1)) * sms)));
+    kern<<<grid, kBThreads, smem, a.stream>>>(a, n_chunks, n_groups, s, counter, part_dB,
+                                              part_dC, part_dA, part_dD, part_db);
     return cudaGetLastError();
   };
+  if (e == cudaSuccess && sg.n_seg > 1)  // aggregates of segments 1 .. n_seg - 1
+    e = staged ? launch(bwd_chunk_kernel<IO, EULER, true, 4, true>, true, sg, tiles + 1,
+                        n_tiles * (sg.n_seg - 1))
+               : launch(bwd_chunk_kernel<IO, EULER, false, 4, true>, false, sg, tiles + 1,
+                        n_tiles * (sg.n_seg - 1));
   if (e == cudaSuccess) {
     if (staged)
-      e = four ? launch(bwd_chunk_kernel<IO, EULER, true, 4>, true)
-               : launch(bwd_chunk_kernel<IO, EULER, true, 3>, true);
+      e = four ? launch(bwd_chunk_kernel<IO, EULER, true, 4>, true, sg, tiles, n_units)
+               : launch(bwd_chunk_kernel<IO, EULER, true, 3>, true, sg, tiles, n_units);
     else
-      e = four ? launch(bwd_chunk_kernel<IO, EULER, false, 4>, false)
-               : launch(bwd_chunk_kernel<IO, EULER, false, 3>, false);
+      e = four ? launch(bwd_chunk_kernel<IO, EULER, false, 4>, false, sg, tiles, n_units)
+               : launch(bwd_chunk_kernel<IO, EULER, false, 3>, false, sg, tiles, n_units);
   }
   if (e == cudaSuccess) {
     const int64_t total = a.batch * a.L * a.N + a.dim * a.N + 2 * a.dim;
     const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, 148 * 16));
-    bwd_reduce_kernel<<<blocks, 256, 0, a.stream>>>(a, n_groups, part_dB, part_dC, part_dA,
-                                                    part_dD, part_db);
+    bwd_reduce_kernel<<<blocks, 256, 0, a.stream>>>(a, n_groups, sg.n_seg, part_dB, part_dC,
+                                                    part_dA, part_dD, part_db);
     e = cudaGetLastError();
   }
   cudaError_t e2 = cudaFreeAsync(ws, a.stream);

@@ -129,3 +129,20 @@ def test_backward_unaligned_inputs(io):
         tol = 1e-5 if (io == "f32" or k not in IO_GRADS) else 1e-2
         err = ((gq - r).abs().max() / r.abs().max().clamp_min(1e-30)).item()
         assert err <= tol, f"{k}: {err:.3g}"
+
+
+@pytest.mark.parametrize("segments", [2, 3, 7])
+@pytest.mark.parametrize("euler", [False, True])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward_time_segments(segments, euler, io, monkeypatch):
+    """The sequence split into time segments: an aggregate pass carries the adjoint of every
+    later segment back to each segment's end (zero-order hold and first-order factors)."""
+    monkeypatch.setenv("SSCAN_BWD_SEGMENTS", str(segments))
+    _check(io, batch=2, L=301 if segments != 7 else 1777, dim=136, N=16, euler=euler, opt=True,
+           what=f"bwd segments={segments} {io} euler={euler}")
+
+
+def test_backward_time_segments_register_path(monkeypatch):
+    """Time segments on the register-load path (N 5) with a ragged last segment."""
+    monkeypatch.setenv("SSCAN_BWD_SEGMENTS", "4")
+    _check("f32", batch=3, L=250, dim=37, N=5, euler=False, opt=True, what="bwd segments N=5")
