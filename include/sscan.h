@@ -137,8 +137,11 @@ sscan_status_t sscan_step(const void* u, const void* delta, const float* A, cons
  *   dh0         : (batch, dim, N) fp32 gradient with respect to the initial state, or NULL
  * Parameter gradients (dA, dB, dC, dD, ddelta_bias) are sums over the other axes, reduced in a
  * fixed order: results are deterministic. Workspace: stream-ordered (cudaMallocAsync) state
- * checkpoints every 16 steps (batch * dim * N floats each) and per-channel-group partial sums
- * of dB, dC. Argument errors are synchronous (SSCAN_ERR_INVALID_ARG).
+ * checkpoints every 16 steps (batch * dim * N floats each), per-channel-group partial sums of
+ * dB, dC, and, when the sequence is split into time segments (fewer batch rows x 32-channel
+ * groups than SMs), per-segment partials and adjoint aggregates. Argument errors are
+ * synchronous (SSCAN_ERR_INVALID_ARG); a bounded wait of the recomputing forward pass that runs
+ * out is reported by sscan_get_device_error, as for sscan_fwd.
  */
 sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias,
@@ -163,7 +166,8 @@ sscan_status_t sscan_bwd(const void* u, const void* delta, const float* A, const
  *   x_prev : (batch, width-1, dim) `dtype`, the width-1 inputs before t = 0 (oldest first), for
  *            continuing a streamed sequence; NULL means zeros
  * 1 <= width <= 64. Asynchronous on `stream`; allocates nothing; argument errors are synchronous
- * (SSCAN_ERR_INVALID_ARG), launch errors SSCAN_ERR_CUDA.
+ * (SSCAN_ERR_INVALID_ARG), launch errors SSCAN_ERR_CUDA; a bounded wait of the tile pipeline
+ * that runs out sets the status word that sscan_get_device_error reports.
  */
 sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bias,
                                  const void* x_prev, int silu_flag, void* y, int64_t batch,
@@ -221,8 +225,9 @@ sscan_status_t sscan_fwd_noalloc(const void* u, const void* delta, const float* 
                                  int64_t N, sscan_dtype_t dtype, cudaStream_t stream);
 
 /* Synchronizes `stream`, then reads and clears the current device's status words (set by
- * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT, by sscan_fwd or
- * sscan_fwd_noalloc calls). Allocates nothing. Returns SSCAN_OK if clear. */
+ * kernels on a device-side error such as SSCAN_ERR_CARRY_TIMEOUT, by any entry point's
+ * kernels: the scans, the step, the backward's recomputing forward, the convolution's tile
+ * pipeline, or sscan_fwd_noalloc's). Allocates nothing. Returns SSCAN_OK if clear. */
 sscan_status_t sscan_get_device_error(cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
