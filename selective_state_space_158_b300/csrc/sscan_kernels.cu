@@ -178,7 +178,7 @@ __device__ __forceinline__ void reduce_transpose(const float (&ys)[TC], float (&
     }
   } else {
     static_assert(G == 4, "G must be 1, 2 or 4");
-    // Round 1 (partner lane ^ 2) keeps the steps whose bit 1 matches g's; round 2 (lane ^ 1)
+    // The exchange with lane ^ 2 keeps the steps whose bit 1 matches g's; the one with lane ^ 1
     // the ones whose bit 0 does.
     const bool hi2 = (g & 2) != 0, hi1 = (g & 1) != 0;
     float r1[TC / 2];
