@@ -36,8 +36,8 @@ namespace {
 
 constexpr int kBT = 16;      // steps per chunk
 constexpr int kBH = kBT / 2; // steps per half-chunk sweep
-constexpr int kMinSegChunks = 8;
-constexpr float kLn2 = 0.6931471805599453f;  // 1 / log2(e)  // shortest time segment of the backward, in chunks
+constexpr int kMinSegChunks = 8;  // shortest time segment of the backward, in chunks
+constexpr float kLn2 = 0.6931471805599453f;  // 1 / log2(e)
 constexpr int kBG = 4;       // lanes per channel
 constexpr int kBK = 4;       // states per lane (N <= 16)
 constexpr int kBThreads = 128;  // three blocks per SM under the 170-register budget
