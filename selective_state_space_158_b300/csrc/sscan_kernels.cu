@@ -147,8 +147,9 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
 }
 
 struct LaneSmem {
-  size_t tile_io, bc_f32, stage, off_stage, off_y, y_warp, off_bar, total;
-  __host__ __device__ LaneSmem(int TC, int W, int CPW, int es, int stages) {
+  size_t tile_io, bc_f32, stage, off_stage, off_y, y_warp, off_tab, tab_warp, off_bar, total;
+  // share: a per-warp [TC][CPW] table of (dt, dt u) pairs that the lanes of a channel share.
+  __host__ __device__ LaneSmem(int TC, int W, int CPW, int es, int stages, bool share) {
     const int CH = W * CPW;
     tile_io = align128(size_t(TC) * CH * es);
     bc_f32 = align128(size_t(TC) * kNP * sizeof(float));
@@ -156,7 +157,9 @@ struct LaneSmem {
     off_stage = 0;
     y_warp = align128(size_t(TC) * CPW * es);            // one warp's y tile
     off_y = size_t(stages) * stage;
-    off_bar = off_y + size_t(2) * W * y_warp;            // [2][W] y tiles
+    off_tab = off_y + size_t(2) * W * y_warp;            // [2][W] y tiles
+    tab_warp = share ? align128(size_t(TC) * CPW * 8) : 0;
+    off_bar = off_tab + size_t(W) * tab_warp;
     total = off_bar + 8 * 8 + 8 * 4 + 16;                // full[8], done[8], ticket
   }
 };
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int W = nthr >> 5, CH = W * CPW;
   const int N = p.N, S = p.stages;
-  const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S);
+  const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S, G == 4);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
   unsigned* done = reinterpret_cast<unsigned*>(smem + lay.off_bar + 8 * 8);
   unsigned* s_ticket = done + 8;
@@ -462,13 +465,22 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       constexpr int NPAIR = kShare ? 1 : TC;
       float2 dtp[NPAIR], dtup[NPAIR];
       float dts[kShare ? TC : 1], dus[kShare ? TC : 1];
+      if constexpr (kShare) {  // lane g publishes its own steps t = g + G k in the warp's table
+        float2* tab = reinterpret_cast<float2*>(smem + lay.off_tab + size_t(warp) * lay.tab_warp);
+        __syncwarp();  // every lane has read the previous chunk's entries
 #pragma unroll
-      for (int t = 0; t < TC; ++t) {
-        if constexpr (kShare) {  // step t belongs to lane t % G of this channel's group
-          const int src = (lane & ~(G - 1)) | (t % G);
-          dts[t] = __shfl_sync(0xffffffffu, own_dt[t / G], src);
-          dus[t] = __shfl_sync(0xffffffffu, own_du[t / G], src);
-        } else {
+        for (int k = 0; k < OWN; ++k) tab[(g + G * k) * CPW + lane / G] = f2(own_dt[k], own_du[k]);
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < TC; ++t) {
+          const float2 v = tab[t * CPW + lane / G];
+          dts[t] = v.x;
+          dus[t] = v.y;
+        }
+      }
+      if constexpr (!kShare) {
+#pragma unroll
+        for (int t = 0; t < TC; ++t) {
           dtp[t] = f2(own_dt[t], own_dt[t]);
           dtup[t] = f2(own_du[t], own_du[t]);
         }
@@ -824,11 +836,13 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   const int W = threads / 32;
   const int CH = W * CPW;
   const int es = a.io == Io::F32 ? 4 : 2;
-  if (stages < 2 || stages > 8) stages = 3;
+  // Two stages for the four-lane 32-step layout (its shared memory then admits seven CTAs per
+  // SM), three otherwise.
+  if (stages < 2 || stages > 8) stages = (G == 4 && TC == 32) ? 2 : 3;
   while (stages > 2 &&
-         LaneSmem(TC, W, CPW, es, stages).total + 128 > size_t(227) * 1024)
+         LaneSmem(TC, W, CPW, es, stages, G == 4).total + 128 > size_t(227) * 1024)
     --stages;
-  const LaneSmem lay(TC, W, CPW, es, stages);
+  const LaneSmem lay(TC, W, CPW, es, stages, G == 4);
   const size_t smem_bytes = lay.total + 128;
   if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
   const int64_t n_cg = (a.dim + CH - 1) / CH;
