@@ -68,7 +68,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.sscan_oracle_conv1d.argtypes = [vp, fp, fp, vp, ci, dp, i64, i64, i64, i64, ci]
     lib.sscan_oracle_conv1d.restype = ci
     lib.sscan_oracle_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, ci, vp, fp,
-                                     dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, ci]
+                                     dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, ci,
+                                     ci]
     lib.sscan_oracle_bwd.restype = ci
     _lib_cache[path] = lib
     return lib
@@ -184,11 +185,12 @@ def conv1d(x, w, bias=None, x_prev=None, silu: bool = True, io: str = "f32", lib
 
 
 def bwd(u, delta, A, B, C, Dskip, z, delta_bias, dy, dh_last=None, softplus: bool = True,
-        h0=None, euler: bool = False, io: str = "f32", lib=None):
+        h0=None, euler: bool = False, io: str = "f32", lib=None, mag: bool = False):
     """Gradients of sum(dy * y) + sum(dh_last * h_last) for the forward of ``fwd`` (see
     ``sscan_oracle_bwd``). dy: (batch, L, dim) io array; dh_last: (batch, dim, N) float32 or
     None. Returns a dict of float64 arrays: du, ddelta, dA, dB, dC, and dz / dD / ddelta_bias /
-    dh0 when z / Dskip / delta_bias / h0 are given."""
+    dh0 when z / Dskip / delta_bias / h0 are given. With ``mag`` the same dict holds each
+    gradient's magnitude (every term taken by its absolute value) instead."""
     lib = lib or load()
     u, delta, dy = _io_array(u, io), _io_array(delta, io), _io_array(dy, io)
     B, C = _io_array(B, io), _io_array(C, io)
@@ -212,7 +214,7 @@ def bwd(u, delta, A, B, C, Dskip, z, delta_bias, dy, dh_last=None, softplus: boo
                               _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
                               _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
                               _ptr(out["ddelta_bias"]), _ptr(out["dh0"]), batch, L, dim, N,
-                              int(io == "bf16"))
+                              int(io == "bf16"), int(bool(mag)))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     return {k: v for k, v in out.items() if v is not None}

@@ -147,7 +147,9 @@ void sscan_oracle_channel_ex(const void *u, const void *delta, const void *z, in
 #if SSCAN_ORACLE_MUTANT != 3
     if (Dskip_d) { /* mutant 3: skip term dropped */
       acc += (double)*Dskip_d * ut;
-      mag += fabs((double)*Dskip_d * ut);
+#if SSCAN_ORACLE_MUTANT != 24
+      mag += fabs((double)*Dskip_d * ut); /* mutant 24: the skip term left out of the magnitude */
+#endif
     }
 #endif
     if (z) {
@@ -321,13 +323,20 @@ int sscan_oracle_conv1d(const void *x, const float *w, const float *bias, const 
  * (dim, N); dB, dC (batch, L, N); dD (dim) if Dskip; dbias (dim) if bias; dh0 (batch, dim, N)
  * if not NULL. dy is (batch, L, dim) io; dh_last (batch, dim, N) fp32 or NULL. Single-threaded
  * (the parameter gradients sum over channels). Returns 0, or -1 on bad sizes.
+ *
+ * mag != 0 computes, in the same outputs, each gradient's magnitude instead: the same sums with
+ * every input, factor and derivative factor replaced by its absolute value, so that every term
+ * enters with its size (the scale that rounding in a finite-precision evaluation of the gradient
+ * is proportional to, as ymag is for y). With every input non-negative and no negative factor
+ * the magnitude equals the gradient.
  */
 int sscan_oracle_bwd(const void *u, const void *delta, const float *A, const void *Bm,
                      const void *Cm, const float *Dskip, const void *z, const float *bias,
                      int softplus_flag, const float *h0, int euler, const void *dy,
                      const float *dh_last, double *du, double *ddelta, double *dA, double *dB,
                      double *dC, double *dD, double *dz, double *dbias, double *dh0,
-                     int64_t batch, int64_t L, int64_t dim, int64_t N, int io_bf16) {
+                     int64_t batch, int64_t L, int64_t dim, int64_t N, int io_bf16, int mag) {
+#define M(v) (mag ? fabs(v) : (v)) /* a leaf of the gradient's terms (its size when mag) */
   if (batch < 0 || L < 0 || dim < 0 || N < 1) return -1;
   memset(dA, 0, sizeof(double) * (size_t)(dim * N));
   memset(dB, 0, sizeof(double) * (size_t)(batch * L * N));
@@ -343,32 +352,36 @@ int sscan_oracle_bwd(const void *u, const void *delta, const float *A, const voi
   for (int64_t b = 0; b < batch; ++b)
     for (int64_t d = 0; d < dim; ++d) {
       const int64_t cbase = b * L * dim + d; /* element (b, 0, d) */
-      const double Dd = Dskip ? (double)Dskip[d] : 0.0;
-      for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? (double)h0[(b * dim + d) * N + n] : 0.0;
+      const double Dd = M(Dskip ? (double)Dskip[d] : 0.0);
+      for (int64_t n = 0; n < N; ++n) hs[n] = M(h0 ? (double)h0[(b * dim + d) * N + n] : 0.0);
       for (int64_t t = 0; t < L; ++t) { /* forward, every state kept */
         const int64_t i = cbase + t * dim;
         const double x = widen(delta, i, io_bf16) + (bias ? (double)bias[d] : 0.0);
         const double dt = softplus_flag ? softplus(x) : x;
-        const double ut = widen(u, i, io_bf16);
+        const double ut = M(widen(u, i, io_bf16));
         double s = Dd * ut;
         for (int64_t n = 0; n < N; ++n) {
-          const double a = euler ? 1.0 + dt * (double)A[d * N + n] : exp(dt * (double)A[d * N + n]);
-          const double hn = a * hs[t * N + n] + dt * widen(Bm, (b * L + t) * N + n, io_bf16) * ut;
+          const double a =
+              M(euler ? 1.0 + dt * (double)A[d * N + n] : exp(dt * (double)A[d * N + n]));
+          const double hn =
+              a * hs[t * N + n] + M(dt) * M(widen(Bm, (b * L + t) * N + n, io_bf16)) * ut;
           hs[(t + 1) * N + n] = hn;
           as[t * N + n] = a;
-          s += widen(Cm, (b * L + t) * N + n, io_bf16) * hn;
+          s += M(widen(Cm, (b * L + t) * N + n, io_bf16)) * hn;
         }
         xs[t] = x;
         dts[t] = dt;
         ss[t] = s;
       }
-      for (int64_t n = 0; n < N; ++n) mu[n] = dh_last ? (double)dh_last[(b * dim + d) * N + n] : 0.0;
+      for (int64_t n = 0; n < N; ++n)
+        mu[n] = M(dh_last ? (double)dh_last[(b * dim + d) * N + n] : 0.0);
       for (int64_t t = L - 1; t >= 0; --t) { /* adjoint sweep */
         const int64_t i = cbase + t * dim;
-        const double ut = widen(u, i, io_bf16), dyt = widen(dy, i, io_bf16), dt = dts[t];
+        const double ut = M(widen(u, i, io_bf16)), dyt = M(widen(dy, i, io_bf16));
+        const double dt = M(dts[t]);
         double ds = dyt;
         if (z) {
-          const double zt = widen(z, i, io_bf16), sg = 1.0 / (1.0 + exp(-zt));
+          const double zr = widen(z, i, io_bf16), sg = 1.0 / (1.0 + exp(-zr)), zt = M(zr);
           ds = dyt * zt * sg;
 #if SSCAN_ORACLE_MUTANT == 23
           dz[i] = dyt * ss[t] * sg; /* mutant: gate derivative taken as the sigmoid alone */
@@ -379,9 +392,9 @@ int sscan_oracle_bwd(const void *u, const void *delta, const float *A, const voi
         if (dD) dD[d] += ds * ut;
         double dut = ds * Dd, ddt = 0.0;
         for (int64_t n = 0; n < N; ++n) {
-          const double Bt = widen(Bm, (b * L + t) * N + n, io_bf16);
-          const double Ct = widen(Cm, (b * L + t) * N + n, io_bf16);
-          const double An = (double)A[d * N + n], a = as[t * N + n];
+          const double Bt = M(widen(Bm, (b * L + t) * N + n, io_bf16));
+          const double Ct = M(widen(Cm, (b * L + t) * N + n, io_bf16));
+          const double An = M((double)A[d * N + n]), a = as[t * N + n];
           const double lam = mu[n] + ds * Ct;
 #if SSCAN_ORACLE_MUTANT == 21
           dC[(b * L + t) * N + n] += ds * hs[t * N + n]; /* mutant: previous state in dC */
@@ -423,4 +436,5 @@ int sscan_oracle_bwd(const void *u, const void *delta, const float *A, const voi
   free(ss);
   free(mu);
   return 0;
+#undef M
 }

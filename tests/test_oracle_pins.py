@@ -576,10 +576,58 @@ def pin_bwd_finite_difference(lib=None):
             assert abs(got - fd) <= 1e-6 * (1 + abs(fd)), (k, idx, got, fd)
 
 
+# ---------------------------------------------------------------------------------------------
+# Magnitudes: the scale of every output's (and gradient's) terms, which the parity metric uses
+# for outputs that cancel. Pinned by what they must be: with no negative term they equal the
+# value itself, and they never fall below its absolute value.
+# ---------------------------------------------------------------------------------------------
+def pin_magnitude_forward(lib=None):
+    rng = np.random.default_rng(51)
+    batch, L, dim, N = 2, 40, 5, 16
+    pos = lambda *s: _f32(np.abs(rng.standard_normal(s)))  # noqa: E731
+    A = _f32(-np.arange(1, N + 1) * np.ones((dim, 1)) * 0.3)
+    args = (pos(batch, L, dim), _f32(rng.standard_normal((batch, L, dim))), A, pos(batch, L, N),
+            pos(batch, L, N), pos(dim), pos(batch, L, dim), _f32(rng.uniform(-3, -1, dim)))
+    # every term non-negative (exp factors, softplus steps, and positive u, B, C, D, z, SiLU(z))
+    y, h, m = oracle.fwd(*args, want_mag=True, lib=lib)
+    np.testing.assert_array_equal(m, y)
+    # random signs: the magnitude bounds the value
+    args = (_f32(rng.standard_normal((batch, L, dim))), _f32(rng.standard_normal((batch, L, dim))),
+            A, _f32(rng.standard_normal((batch, L, N))), _f32(rng.standard_normal((batch, L, N))),
+            _f32(rng.standard_normal(dim)), _f32(rng.standard_normal((batch, L, dim))),
+            _f32(rng.uniform(-3, -1, dim)))
+    y, h, m = oracle.fwd(*args, want_mag=True, lib=lib)
+    assert np.all(m >= np.abs(y)) and np.all(m > 0)
+
+
+def pin_magnitude_backward(lib=None):
+    for softplus, euler in [(True, False), (False, True)]:
+        c, dy, dh = _bwd_case(52, softplus, euler, True)
+        g = oracle.bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], c.get("D"), c.get("z"),
+                       c.get("bias"), dy, dh, softplus=softplus, h0=c.get("h0"), euler=euler,
+                       lib=lib)
+        m = oracle.bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], c.get("D"), c.get("z"),
+                       c.get("bias"), dy, dh, softplus=softplus, h0=c.get("h0"), euler=euler,
+                       lib=lib, mag=True)
+        for k in g:
+            assert np.all(m[k] >= np.abs(g[k]) * (1 - 1e-12)), (k, softplus, euler)
+        # no negative term anywhere: non-negative inputs and a non-negative A (a growing state,
+        # fine for 13 steps), positive steps; then every magnitude equals its gradient
+        pc = {k: _f32(np.abs(v)) for k, v in c.items()}
+        pdy, pdh = _f32(np.abs(dy)), _f32(np.abs(dh))
+        gp = oracle.bwd(pc["u"], pc["delta"], pc["A"], pc["B"], pc["C"], pc["D"], pc["z"], None,
+                        pdy, pdh, softplus=softplus, h0=pc["h0"], euler=euler, lib=lib)
+        mp = oracle.bwd(pc["u"], pc["delta"], pc["A"], pc["B"], pc["C"], pc["D"], pc["z"], None,
+                        pdy, pdh, softplus=softplus, h0=pc["h0"], euler=euler, lib=lib, mag=True)
+        for k in gp:
+            np.testing.assert_allclose(mp[k], gp[k], rtol=1e-12, atol=0, err_msg=k)
+
+
 PINS = [pin_worked_example, pin_selective_demo, pin_lti_convolution, pin_matrix_form,
         pin_associativity, pin_delta_zero, pin_skip_gate, pin_softplus, pin_bf16_widening,
         pin_h0_free_decay, pin_h0_superposition, pin_h0_split_sequence, pin_euler_lti,
-        pin_conv1d_numpy, pin_conv1d_stream, pin_bwd_autograd, pin_bwd_finite_difference]
+        pin_conv1d_numpy, pin_conv1d_stream, pin_bwd_autograd, pin_bwd_finite_difference,
+        pin_magnitude_forward, pin_magnitude_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -628,6 +676,7 @@ MUTANTS = {
     21: "backward: dC from the previous state",
     22: "backward: softplus derivative dropped",
     23: "backward: gate derivative taken as the sigmoid alone",
+    24: "magnitude: the skip term left out",
 }
 
 
