@@ -2,8 +2,19 @@
 """Benchmark of the S6 selective-scan forward (libsscan) on B300.
 
 One step = one selective-scan forward over the whole workload (softplus, discretisation,
-recurrence, readout, skip, gate, h_last) = one kernel launch. Default workload: fp32, batch 8,
-L 2048, D 1536 (d_model 768, expand 2), N 16, z gate, D skip, h_last returned.
+recurrence, readout, skip, gate, h_last): the library's kernels for one sscan_fwd call.
+
+Headline workload (default): the largest single-GPU workload, the long sequence, bf16 io with
+fp32 state, batch 1, L 1,048,576, D 1536, N 16, h_last returned. The same JSON line carries, under
+"configs", the other full-size workloads with L >= 2048 (fp32 b8 L2048 D1536; bf16 b16 L4096
+D2048; bf16 b4 L8192 D5120), each timed over a region of at least 200 ms, with its own roofline.
+
+Rooflines. The HBM bound divides the algorithmic bytes (inputs read once, outputs written once) by
+the measured copy bandwidth (MEASURED_PEAKS.json). The compute ("alu") bound counts, per state
+update, one SFU exponential and four FP32-pipe operations; its denominators are measured live, at
+the start of the run, by the library's own issue-rate probes (libsscan_peaks: ex2.approx and FFMA
+throughput per SM and clock), times the SM count and the maximum SM clock. The bound of a workload
+is the slower of the two.
 
 Prints ONE JSON line (rank 0). Under torchrun with N ranks every rank runs its own full replica
 of the workload on its own GPU (the batch rows and channels are independent; no data-path
@@ -13,13 +24,16 @@ slowest rank's time is used: value = N * units / max_time ("scaling": "weak").
 --impl reference times the fp64 CPU oracle (the correctness reference) on a bounded sample of
 the same workload per step, on this machine's host cores.
 
+--mode peaks prints the issue-rate probes' results (per SM and clock, and per second at the
+maximum clock) as one JSON line.
+
 --mode conv times the causal depthwise Conv1d + SiLU (sscan_conv1d_silu) over the workload's
 (batch, L, dim) in its io type; the roofline is HBM on the input read once, the output written
 once and the tiles' halos.
 
 --mode bwd times the backward pass (sscan_bwd: checkpoints, adjoint sweep, reductions) on the
 workload with random dy and dh_last; its compute roofline counts the FP32-pipe operations of a
-recompute plus an adjoint step per update (16) against 128 per clock per SM.
+recompute plus an adjoint step per update (16) against the measured FFMA rate.
 
 --mode decode times the single-step recurrence (sscan_step) on the workload's batch, channels
 and state size instead: one step per token, the state read and written in place, as K
@@ -43,23 +57,28 @@ sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan fwd GB/s and (B·L·D·N)/s on 1 B300; % of HBM/SFU roofline"
 UNIT = "(B*L*D*N)/s"
-SFU_EX2_PER_CLK_PER_SM = 32  # MUFU.EX2 lanes per SM per clock on B300 (measured by our probe)
 FALLBACK_HBM_GBS = 6400.0
+FP32_OPS_PER_UPDATE = 4  # dt*A, dt*u*B, the state FMA, the readout FMA
+MIN_REGION_MS = 200.0    # each extra workload is timed over at least this much device time
+EXTRA_WORKLOADS = ("fp32", "bf16", "wide")
 L2_BYTES = 126 * 2**20
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["lib", "reference"], default="lib")
-    ap.add_argument("--workload", default="fp32")
+    ap.add_argument("--workload", default="long")
+    ap.add_argument("--L", type=int, default=0, help="override the workload's L (profiling)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["scan", "decode", "conv", "bwd"], default="scan")
+    ap.add_argument("--mode", choices=["scan", "decode", "conv", "bwd", "peaks"], default="scan")
     ap.add_argument("--conv-width", type=int, default=4)
     return ap.parse_args()
 
@@ -540,13 +559,113 @@ def run_bwd(args, w):
     print(json.dumps(line), flush=True)
 
 
+def measure_rates(index: int = 0) -> dict:
+    """Issue rates of this GPU's SMs from the library's probes (libsscan_peaks): ex2.approx,
+    scalar FFMA, packed FFMA2, and the scan's per-update mix (one ex2 + four FP32 operations) in
+    both forms; per SM and clock (clock-independent: cycles counted on the SM)."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from selective_state_space_158_b300 import build
+
+    lib = ctypes.CDLL(build.PEAKS_LIB)
+    fn = lib.sscan_peaks_probe
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(index).multi_processor_count
+    blocks, iters = 2 * sms, 4096
+    out = {}
+    with torch.cuda.device(index):
+        for kind, name in enumerate(["ex2", "ffma", "ffma2", "mix_packed", "mix_scalar"]):
+            cyc = np.zeros(blocks, dtype=np.int64)
+            e, f = ctypes.c_int(), ctypes.c_int()
+            rc = fn(kind, blocks, iters, cyc.ctypes.data, ctypes.byref(e), ctypes.byref(f))
+            if rc != 0:
+                raise RuntimeError(f"rate probe {name} failed: CUDA error {rc}")
+            med = float(np.median(cyc))
+            out[name] = {"ex2_per_clk_sm": 1024 * iters * e.value / med,
+                         "fp32_per_clk_sm": 1024 * iters * f.value / med,
+                         "cycles_median": med, "cycles_spread": [int(cyc.min()), int(cyc.max())]}
+    return out
+
+
+def update_peak(rates: dict, sms: int, mhz: float) -> dict:
+    """The compute roofline of the scan: per update one SFU ex2 and four FP32-pipe operations,
+    at the measured ex2 rate and the better of the measured FFMA / FFMA2 rates."""
+    r_ex2 = rates["ex2"]["ex2_per_clk_sm"]
+    r_fma = max(rates["ffma"]["fp32_per_clk_sm"], rates["ffma2"]["fp32_per_clk_sm"])
+    per_clk = min(r_ex2, r_fma / FP32_OPS_PER_UPDATE)
+    return {"updates_per_s": per_clk * sms * mhz * 1e6, "sms": sms, "mhz": mhz,
+            "ex2_per_clk_sm": r_ex2,
+            "fp32_per_clk_sm": r_fma, "updates_per_clk_sm": per_clk,
+            "binding_pipe": "SFU" if r_ex2 <= r_fma / FP32_OPS_PER_UPDATE else "FP32",
+            "mix_updates_per_clk_sm": rates["mix_packed"]["ex2_per_clk_sm"],
+            "source": f"libsscan_peaks probes on this GPU x {sms} SMs x {mhz:.0f} MHz (max SM "
+                      f"clock)"}
+
+
+def scan_roofline(w, sec_per_launch: float, peak: dict, hbm_gbs: float, peak_src: str,
+                  traffic, clocks=None) -> dict:
+    bytes_ = w.io_bytes()
+    gbs = bytes_ / sec_per_launch / 1e9
+    ups = w.elems / sec_per_launch
+    t_hbm = bytes_ / (hbm_gbs * 1e9)
+    t_alu = w.elems / peak["updates_per_s"]
+    if t_hbm >= t_alu:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": gbs / hbm_gbs, "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"}
+    else:
+        roof = {"bound": "alu", "achieved": ups / 1e9, "peak": peak["updates_per_s"] / 1e9,
+                "unit": "G state updates/s (1 SFU ex2 + 4 FP32 ops each)",
+                "frac": ups / peak["updates_per_s"], "traffic": traffic,
+                "peak_source": peak["source"]}
+    roof["hbm_frac"] = gbs / hbm_gbs
+    roof["alu_frac"] = ups / peak["updates_per_s"]
+    roof["algorithmic_bytes"] = bytes_
+    roof["t_hbm_ms"] = t_hbm * 1e3
+    roof["t_alu_ms"] = t_alu * 1e3
+    if clocks and clocks.get("sm_mhz"):
+        at_obs = peak["updates_per_clk_sm"] * peak["sms"] * clocks["sm_mhz"] * 1e6
+        roof["alu_frac_at_observed_clock"] = ups / at_obs
+    return roof
+
+
+def launches_per_step(w) -> int:
+    """The library's kernels per sscan_fwd call: the scan, plus the pass that widens B and C to
+    fp32 rows of 16 states when they are bf16 or N < 16."""
+    return 1 + (1 if (w.io != "f32" or w.N != 16) else 0)
+
+
+def run_peaks(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    rates = measure_rates(0)
+    props = torch.cuda.get_device_properties(0)
+    _, mhz, _ = peaks()
+    pk = update_peak(rates, props.multi_processor_count, mhz)
+    line = {"metric": "issue rates per SM and clock (libsscan_peaks)", "gpu": props.name,
+            "sms": props.multi_processor_count, "sm_max_mhz": mhz, "rates": rates,
+            "scan_update_peak": pk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from selective_state_space_158_b300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
+    if args.L:
+        w = w.replace(L=args.L)
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.mode == "peaks":
+        run_peaks(args)
         return
     if args.mode == "decode":
         run_decode(args, w)
@@ -571,20 +690,28 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     binding.load()  # fails loudly if the library is missing
 
-    x = make_inputs(w, device=dev)
-    y = torch.empty_like(x["u"])
-    h = torch.empty((w.batch, w.dim, w.N), dtype=torch.float32, device=dev)
+    hbm_gbs, sm_max_mhz, peak_src = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    rates = measure_rates(local)
+    upeak = update_peak(rates, sms, sm_max_mhz)
     stream = torch.cuda.Stream(dev)
-
-    def step():
-        binding.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x.get("D"), x.get("z"),
-                    x.get("delta_bias"), y=y, h_last=h, stream=stream)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    def timed(K):
+    def prepare(wk):
+        x = make_inputs(wk, device=dev)
+        y = torch.empty_like(x["u"])
+        h = torch.empty((wk.batch, wk.dim, wk.N), dtype=torch.float32, device=dev)
+
+        def step():
+            binding.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x.get("D"), x.get("z"),
+                        x.get("delta_bias"), y=y, h_last=h, stream=stream)
+        return x, y, h, step
+
+    def timed(step, K):
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         barrier()
@@ -596,61 +723,45 @@ def main():
             ev1.record(stream)
             torch.cuda.synchronize(dev)
         barrier()
-        ms = ev0.elapsed_time(ev1)
-        return ms, cs
+        return ev0.elapsed_time(ev1), cs
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(dev)
-    if binding.device_error(stream) != 0:
-        raise RuntimeError("device-side error during warm-up")
-    ms, cs = timed(args.steps)
-    remeasured = False
-    if cs.rejected():
-        ms, cs = timed(args.steps)
-        remeasured = True
-    if binding.device_error(stream) != 0:
-        raise RuntimeError("device-side error during the timed region")
-    ms_max = max_over_ranks(ms, world, dev)
+    def measure(step, K):
+        ms, cs = timed(step, K)
+        remeasured = False
+        if cs.rejected():
+            ms, cs = timed(step, K)
+            remeasured = True
+        if binding.device_error(stream) != 0:
+            raise RuntimeError("device-side error during the timed region")
+        clocks = cs.summary()
+        if remeasured:
+            clocks["note"] = "first measurement rejected by clock check; re-measured once"
+        return max_over_ranks(ms, world, dev), clocks
+
+    def warm(step, n):
+        for _ in range(max(3, n)):
+            step()
+        torch.cuda.synchronize(dev)
+        if binding.device_error(stream) != 0:
+            raise RuntimeError("device-side error during warm-up")
+
+    # ---- headline workload: exactly --steps steps ----
+    x, y, h, step = prepare(w)
+    warm(step, args.warmup)
+    ms_max, clocks = measure(step, args.steps)
     sec_per_step = ms_max / 1e3 / args.steps
     value = whole_job_rate(w.elems, world, sec_per_step)
-
-    # ---- roofline of the (only) kernel: one launch per step, timed on its own stream ----
-    hbm_gbs, sm_max_mhz, peak_src = peaks()
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    alu_peak = sms * SFU_EX2_PER_CLK_PER_SM * sm_max_mhz * 1e6  # ex2 (= updates) per second
-    per_launch_s = ms / 1e3 / args.steps
-    bytes_ = w.io_bytes()
-    gbs = bytes_ / per_launch_s / 1e9
-    t_hbm = bytes_ / (hbm_gbs * 1e9)
-    t_alu = w.elems / alu_peak
-    traffic = recorded_traffic(args.workload)
-    if t_hbm >= t_alu:
-        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": gbs / hbm_gbs, "traffic": traffic,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"}
-    else:
-        ach = w.elems / per_launch_s
-        roof = {"bound": "alu", "achieved": ach / 1e9, "peak": alu_peak / 1e9,
-                "unit": "G ex2/s (SFU)", "frac": ach / alu_peak, "traffic": traffic,
-                "peak_source": f"{sms} SMs x {SFU_EX2_PER_CLK_PER_SM} ex2/clk x {sm_max_mhz:.0f} MHz"}
-    roof["hbm_frac"] = gbs / hbm_gbs
-    roof["sfu_frac"] = (w.elems / per_launch_s) / alu_peak
-    clocks = cs.summary()
-    if clocks.get("sm_mhz"):
-        roof["sfu_frac_at_observed_clock"] = (w.elems / per_launch_s) / (
-            sms * SFU_EX2_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6)
-
+    roof = scan_roofline(w, sec_per_step, upeak, hbm_gbs, peak_src,
+                         recorded_traffic(args.workload), clocks)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.io, "data": "synthetic (seeded)",
-        "config": config_of(w), "gbs": gbs * world, "gpu_launches": args.steps,
+        "config": config_of(w), "gbs": w.io_bytes() / sec_per_step / 1e9 * world,
+        "gpu_launches": args.steps * launches_per_step(w),
         "roofline": roof, "clocks": clocks,
+        "peaks": {"update_peak": upeak, "probes": rates},
     }
-    if remeasured:
-        line["clocks"]["note"] = "first measurement rejected by clock check; re-measured once"
 
     # ---- end to end through the host-buffer C entry point ----
     if not args.no_e2e:
@@ -663,8 +774,7 @@ def main():
                              xh.get("z"), xh.get("delta_bias"), y=yh, h_last=hh, device=local,
                              stream=stream)
 
-        for _ in range(2):
-            e2e_step()
+        e2e_step()
         K2 = max(3, args.e2e_steps)
         barrier()
         t0 = time.perf_counter()
@@ -681,9 +791,38 @@ def main():
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "steps": K2, "ms_per_step": el / K2 * 1e3,
                        "api": "sscan_fwd_host (pinned host buffers, copies inside the region)"}
+        del xh, yh, hh
 
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+    del x, y, h, step
+    torch.cuda.empty_cache()
+
+    # ---- the other full-size workloads, each over >= MIN_REGION_MS of device time ----
+    if not args.no_configs:
+        line["configs"] = {}
+        for key in EXTRA_WORKLOADS:
+            if key == args.workload:
+                continue
+            wk = WORKLOADS[key]
+            xk, yk, hk, stepk = prepare(wk)
+            warm(stepk, 3)
+            t1, _ = timed(stepk, 3)
+            K = max(5, math.ceil(MIN_REGION_MS / max(t1 / 3, 1e-3)))
+            K = int(max_over_ranks(K, world, dev))
+            msk, ck = measure(stepk, K)
+            sk = msk / 1e3 / K
+            line["configs"][key] = {
+                "workload": wk.name, "ms_per_step": msk / K, "steps": K,
+                "timed_ms": msk, "value": whole_job_rate(wk.elems, world, sk), "unit": UNIT,
+                "gbs": wk.io_bytes() / sk / 1e9 * world, "dtype": wk.io,
+                "gpu_launches": K * launches_per_step(wk),
+                "roofline": scan_roofline(wk, sk, upeak, hbm_gbs, peak_src,
+                                          recorded_traffic(key), ck),
+                "clocks": ck, "config": config_of(wk)}
+            del xk, yk, hk, stepk
+            torch.cuda.empty_cache()
+
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -7,6 +7,7 @@ CUDA device is present, the calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -37,6 +38,17 @@ _CONV_ARGS = [_vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64, _int, _vp]
 # ddelta_bias, dh0, batch, L, dim, N, dtype, stream.
 _BWD_ARGS = [_vp] * 9 + [_vp, _int] + [_vp] * 11 + [_i64] * 4 + [_int, _vp]
 _BWD_ARGS[8] = _int  # softplus_flag
+
+
+class Tuning(ctypes.Structure):
+    """sscan_tuning_t (include/sscan_tuning.h): layout overrides and the fault-injection hook."""
+    _fields_ = [("states_per_lane", ctypes.c_int), ("segments", ctypes.c_int),
+                ("threads", ctypes.c_int), ("stages", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("force_plain", ctypes.c_int), ("bwd_segments", ctypes.c_int),
+                ("conv_plain", ctypes.c_int), ("test_skip_publish", ctypes.c_int)]
+
+
+_TUNING_P = ctypes.POINTER(Tuning)
 SIGNATURES = {
     "sscan_fwd": (_FWD_ARGS, _int),
     "sscan_bwd": (_BWD_ARGS, _int),
@@ -48,6 +60,9 @@ SIGNATURES = {
     "sscan_get_device_error": ([_vp], _int),
     "sscan_status_string": ([_int], ctypes.c_char_p),
     "sscan_release": ([], _int),
+    "sscan_set_tuning": ([_TUNING_P], _int),
+    "sscan_get_tuning": ([_TUNING_P], _int),
+    "sscan_exp2_accurate": ([_vp, _vp, _i64, _vp], _int),
 }
 
 _lib = None
@@ -312,6 +327,39 @@ def device_error(stream=None, device=None) -> int:
     dev = device if device is not None else torch.cuda.current_device()
     with torch.cuda.device(dev):
         return lib.sscan_get_device_error(_stream_handle(stream, dev))
+
+
+@contextlib.contextmanager
+def tuning(**fields):
+    """Within the block, the library uses the given layout overrides (fields of
+    ``sscan_tuning_t``; the others keep their automatic choice); the previous setting is restored
+    on exit. For tests and tuning sweeps."""
+    lib = load()
+    prev = Tuning()
+    _check(lib.sscan_get_tuning(ctypes.byref(prev)), "sscan_get_tuning")
+    t = Tuning(test_skip_publish=-1)
+    for k, v in fields.items():
+        if k not in dict(Tuning._fields_):
+            raise KeyError(f"unknown tuning field {k}")
+        setattr(t, k, int(v))
+    _check(lib.sscan_set_tuning(ctypes.byref(t)), "sscan_set_tuning")
+    try:
+        yield
+    finally:
+        _check(lib.sscan_set_tuning(ctypes.byref(prev)), "sscan_set_tuning")
+
+
+def exp2_accurate(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """2^x with the library's accurate exponential (``sscan_exp2_accurate``); float32 CUDA."""
+    lib = load()
+    if x.dtype != torch.float32 or x.device.type != "cuda" or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        code = lib.sscan_exp2_accurate(_ptr(x), _ptr(y), x.numel(),
+                                       _stream_handle(stream, x.device))
+    _check(code, "sscan_exp2_accurate")
+    return y
 
 
 def status_string(code: int) -> str:

@@ -1,4 +1,5 @@
-"""Builds libsscan.so in-tree with nvcc for sm_103a (B300)."""
+"""Builds libsscan.so (and the rate-probe library libsscan_peaks.so) in-tree with nvcc for
+sm_103a (B300)."""
 from __future__ import annotations
 
 import os
@@ -9,6 +10,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsscan.so")
+# Issue-rate microbenchmarks (the compute rooflines' denominators); not part of the scan library.
+PEAKS_LIB = os.path.join(PKG, "libsscan_peaks.so")
+PEAKS_SOURCES = ["sscan_peaks.cu"]
 SOURCES = ["sscan_api.cu", "sscan_kernels.cu", "sscan_noalloc.cu", "sscan_conv.cu",
            "sscan_bwd.cu"]
 HEADERS = ["sscan_device.cuh", "sscan_internal.h"]
@@ -28,26 +32,31 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str, sources) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    deps.append(os.path.join(ROOT, "include", "sscan.h"))
+    t = os.path.getmtime(lib)
+    deps = [os.path.join(CSRC, f) for f in list(sources) + HEADERS]
+    deps += [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile the library if any source is newer than it; returns the .so path."""
-    if not force and not _stale():
-        return LIB
-    tmp = LIB + ".tmp"
+def _compile(lib: str, sources, verbose: bool, extra_flags) -> None:
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"),
-           "-o", tmp, *[os.path.join(CSRC, f) for f in SOURCES]]
+           "-o", tmp, *[os.path.join(CSRC, f) for f in sources]]
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile the library (and the rate probes) if any source is newer; returns the .so path."""
+    if force or _stale(LIB, SOURCES):
+        _compile(LIB, SOURCES, verbose, extra_flags)
+    if force or _stale(PEAKS_LIB, PEAKS_SOURCES):
+        _compile(PEAKS_LIB, PEAKS_SOURCES, verbose, extra_flags)
     return LIB
 
 

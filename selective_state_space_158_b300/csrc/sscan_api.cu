@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "../../include/sscan.h"
+#include "../../include/sscan_tuning.h"
 #include "sscan_internal.h"
 
 namespace {
@@ -44,13 +45,10 @@ unsigned int* status_word(int dev) {
   return s.status;
 }
 
-// The TMA-staged kernel when the arguments allow it, else the plain-load kernel.
-cudaError_t launch_forward(const sscan::FwdArgs& a) {
-  const char* force = std::getenv("SSCAN_PATH");
-  const bool want_simple = force && std::strcmp(force, "simple") == 0;
-  if (!want_simple && sscan::tma_path_ok(a)) return sscan::launch_tma(a, sscan::tuning_from_env());
-  return sscan::launch_simple(a);
-}
+std::mutex g_tune_mu;
+sscan::Tuning g_tune;  // sscan_set_tuning's setting, process-wide
+
+using sscan::launch_forward;
 
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
   if (a < 0 || b < 0) return false;
@@ -62,6 +60,11 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 }  // namespace
 
 namespace sscan {
+
+Tuning current_tuning() {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return g_tune;
+}
 
 // Shared validation of sizes and pointer presence; fills the element counts.
 int check_fwd_args(const void* u, const void* delta, const float* A, const void* B,
@@ -95,6 +98,52 @@ sscan_status_t check_args(const void* u, const void* delta, const float* A, cons
 }  // namespace
 
 extern "C" {
+
+sscan_status_t sscan_set_tuning(const sscan_tuning_t* t) {
+  sscan::Tuning n;
+  if (t) {
+    const int k = t->states_per_lane;
+    if ((k != 0 && k != 4 && k != 8 && k != 16) || t->segments < 0 || t->threads < 0 ||
+        t->threads > 256 || t->threads % 32 != 0 || t->stages < 0 || t->stages > 8 ||
+        t->stages == 1 || (t->chunk != 0 && t->chunk != 16 && t->chunk != 32) ||
+        t->bwd_segments < 0 || t->test_skip_publish < -1)
+      return SSCAN_ERR_INVALID_ARG;
+    n.states_per_lane = k;
+    n.segments = t->segments;
+    n.threads = t->threads;
+    n.stages = t->stages;
+    n.chunk = t->chunk;
+    n.force_plain = t->force_plain != 0;
+    n.bwd_segments = t->bwd_segments;
+    n.conv_plain = t->conv_plain != 0;
+    n.skip_publish = t->test_skip_publish;
+  }
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune = n;
+  return SSCAN_OK;
+}
+
+sscan_status_t sscan_exp2_accurate(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return SSCAN_ERR_INVALID_ARG;
+  if (n == 0) return SSCAN_OK;
+  if (current_device() < 0) return SSCAN_ERR_CUDA;
+  return sscan::launch_exp2_accurate(x, y, n, stream) == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
+
+sscan_status_t sscan_get_tuning(sscan_tuning_t* t) {
+  if (!t) return SSCAN_ERR_INVALID_ARG;
+  const sscan::Tuning c = sscan::current_tuning();
+  t->states_per_lane = c.states_per_lane;
+  t->segments = c.segments;
+  t->threads = c.threads;
+  t->stages = c.stages;
+  t->chunk = c.chunk;
+  t->force_plain = c.force_plain;
+  t->bwd_segments = c.bwd_segments;
+  t->conv_plain = c.conv_plain;
+  t->test_skip_publish = c.skip_publish;
+  return SSCAN_OK;
+}
 
 const char* sscan_status_string(sscan_status_t s) {
   switch (s) {

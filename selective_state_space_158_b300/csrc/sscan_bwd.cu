@@ -48,7 +48,7 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + ex2(-x
 template <bool EULER>
 __device__ __forceinline__ float factor(float dt, float a2) {
   // a2 = A log2e (zero-order hold) or A (first order)
-  return EULER ? fmaf(dt, a2, 1.f) : ex2(fmaf(dt, a2, kEx2ArgShift));
+  return EULER ? fmaf(dt, a2, 1.f) : ex2(dt * a2);
 }
 
 // ---- the adjoint sweep over chunks in reverse ------------------------------------------------
@@ -605,7 +605,7 @@ cudaError_t launch_bwd_typed(const BwdArgs& a) {
     const int64_t resident = int64_t(3) * sms;
     int64_t want = n_tiles >= sms ? 1 : (2 * resident + n_tiles - 1) / n_tiles;
     want = std::min<int64_t>(want, std::max(1, n_chunks / kMinSegChunks));
-    if (const char* v = std::getenv("SSCAN_BWD_SEGMENTS")) want = std::max(1, std::atoi(v));
+    if (const int v = current_tuning().bwd_segments; v > 0) want = v;
     want = std::min<int64_t>(want, n_chunks);
     sg.seg_chunks = int((n_chunks + want - 1) / want);
     sg.n_seg = (n_chunks + sg.seg_chunks - 1) / sg.seg_chunks;

@@ -366,7 +366,7 @@ bool conv_tma_ok(const ConvArgs& a, int es) {
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   return a.width <= kMaxTmaWidth && (a.dim * es) % 16 == 0 && al(a.x) && al(a.y) &&
          a.dim <= INT32_MAX && a.L + kTileT < INT32_MAX && a.batch <= INT32_MAX &&
-         std::getenv("SSCAN_CONV_PLAIN") == nullptr;
+         !current_tuning().conv_plain;
 }
 
 template <typename IO>

@@ -42,13 +42,37 @@ __device__ __forceinline__ float2 log1p_unit2(float2 s) {
   return __fmul2_rn(s, acc);
 }
 
-// Argument shift for the decay factor 2^(dt * A * log2 e). Measured on B300 (sm_103a), the SFU's
-// ex2.approx.ftz.f32 returns results that are on average 0.1-0.2 ulp low for arguments in
-// [-3e-3, 0) and up to 0.5 ulp low near -1e-2. A decay factor is multiplied into the state at
-// every step, so a consistently low factor compounds over the state's memory (hundreds to
-// thousands of steps for small dt). Adding 1e-8 to the argument (for free: the product becomes
-// an FMA) centres the error on zero for the slow-decay arguments where compounding matters.
-constexpr float kEx2ArgShift = 1.0e-8f;
+// 2^x on the FMA pipe, accurate to about one ulp and unbiased (the fp32 path's decay over a
+// whole chunk, where the SFU's approximate exponential would otherwise enter the state once per
+// step and its rounding, which leans low for small arguments, would compound over the state's
+// memory). Range reduction after Cody and Waite: k = rint(x) by the 1.5 * 2^23 rounding constant
+// (exact for |x| < 2^22), f = x - k in [-1/2, 1/2] exactly; 2^f by a degree-6 polynomial from
+// Chebyshev interpolation (csrc/gen_exp2_poly.py regenerates it: relative error 1.04e-7 for an
+// unfused fp32 evaluation, mean signed error 1.2e-9); 2^k enters through the exponent field.
+// x is clamped to [-125, 125]: results below 2^-125 are not needed (they multiply a state that
+// has decayed away), and no result is denormal or infinite.
+__device__ __forceinline__ float2 exp2_poly2(float2 f) {
+  constexpr float c[7] = {1.000000000e+00f, 6.931471825e-01f, 2.402265072e-01f,
+                          5.550327152e-02f, 9.618056938e-03f, 1.340042800e-03f,
+                          1.546144485e-04f};
+  float2 p = f2(c[6], c[6]);
+#pragma unroll
+  for (int i = 5; i >= 0; --i) p = __ffma2_rn(p, f, f2(c[i], c[i]));
+  return p;
+}
+__device__ __forceinline__ float2 exp2_acc2(float2 x) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  x = f2(fminf(fmaxf(x.x, -125.f), 125.f), fminf(fmaxf(x.y, -125.f), 125.f));
+  const float2 t = __fadd2_rn(x, f2(kRound, kRound));                    // rint(x) + kRound
+  const float2 kf = __fadd2_rn(t, f2(-kRound, -kRound));                 // rint(x), exact
+  const float2 f = __ffma2_rn(kf, f2(-1.f, -1.f), x);                    // x - rint(x), exact
+  const float2 p = exp2_poly2(f);
+  const int kx = __float_as_int(t.x) - __float_as_int(kRound);
+  const int ky = __float_as_int(t.y) - __float_as_int(kRound);
+  return f2(__int_as_float(__float_as_int(p.x) + (kx << 23)),
+            __int_as_float(__float_as_int(p.y) + (ky << 23)));
+}
+__device__ __forceinline__ float exp2_acc(float x) { return exp2_acc2(f2(x, 0.f)).x; }
 
 // softplus on a pair: max(x, 0) + log1p(exp(-|x|)); one SFU exponential per element.
 __device__ __forceinline__ float2 softplus2(float2 x) {

@@ -38,14 +38,22 @@ struct FwdArgs {
   bool* scratch_short = nullptr;
 };
 
-// Tuning knobs of the TMA-staged kernel. Zero fields mean "choose automatically".
-struct TmaTuning {
+// Layout overrides (sscan_set_tuning, include/sscan_tuning.h). Zero fields mean "choose
+// automatically"; skip_publish -1 means the fault-injection hook is off.
+struct Tuning {
   int states_per_lane = 0;    // K: states of one channel a lane holds (4, 8 or 16)
   int segments = 0;           // time segments run by different CTAs (chunk carry)
   int threads = 0;            // threads per CTA (multiple of 32, <= 256)
   int stages = 0;             // TMA pipeline depth
   int chunk = 0;              // steps per chunk with four lanes per channel (16 or 32)
+  int force_plain = 0;        // forward: plain-load kernel only
+  int bwd_segments = 0;       // backward: time segments
+  int conv_plain = 0;         // Conv1d: register-window kernel only
+  int skip_publish = -1;      // test hook: this segment never publishes its aggregate
 };
+
+// The setting sscan_set_tuning installed (a copy, taken under the setting's lock).
+Tuning current_tuning();
 
 // Size checks shared by the C entry points; fills the element counts (batch*L*dim, batch*L*N).
 int check_fwd_args(const void* u, const void* delta, const float* A, const void* B,
@@ -65,10 +73,14 @@ bool tma_path_ok(const FwdArgs& a);
 
 // Launchers. Return cudaSuccess or the launch error.
 cudaError_t launch_simple(const FwdArgs& a);
-cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& t);
-cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& t);
+cudaError_t launch_tma(const FwdArgs& a, const Tuning& t);
+cudaError_t launch_lane(const FwdArgs& a, const Tuning& t);
+// The TMA-staged kernel when the arguments (and the tuning) allow it, else the plain-load one.
+cudaError_t launch_forward(const FwdArgs& a);
 // One step of the recurrence for every (batch, channel); h_last is the state, read and written.
 cudaError_t launch_step(const FwdArgs& a);
+// y = 2^x element-wise with the accurate exponential (exp2_acc).
+cudaError_t launch_exp2_accurate(const float* x, float* y, int64_t n, cudaStream_t stream);
 
 // Causal depthwise convolution over time + SiLU (sscan_conv1d_silu), arguments validated.
 struct ConvArgs {
@@ -115,9 +127,5 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 cudaError_t launch_bwd(const BwdArgs& a);
-
-// Reads SSCAN_K / SSCAN_THREADS / SSCAN_STAGES / SSCAN_SEGMENTS / SSCAN_TC from the environment
-// (0: unset).
-TmaTuning tuning_from_env();
 
 }  // namespace sscan

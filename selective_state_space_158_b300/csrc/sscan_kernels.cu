@@ -52,7 +52,20 @@ __global__ void __launch_bounds__(128) sscan_simple_kernel(
   }
   const float bs = bias ? bias[d] : 0.f;
   const float Dd = Dskip ? Dskip[d] : 0.f;
+  // fp32 zero-order hold: the decay over every 16-step block is re-anchored (see
+  // sscan_lane_kernel): hs is the block's start state, R the product of its per-step factors,
+  // S its summed step.
+  constexpr bool kAnchor = std::is_same<IO, float>::value && !EULER;
+  float hs[kAnchor ? kNP : 1], R[kAnchor ? kNP : 1], S = 0.f;
   for (int64_t t = 0; t < L; ++t) {
+    if (kAnchor && t % 16 == 0) {
+#pragma unroll
+      for (int n = 0; n < (kAnchor ? kNP : 1); ++n) {
+        hs[n] = h[n];
+        R[n] = 1.f;
+      }
+      S = 0.f;
+    }
     if (h_ckpt && t % 16 == 0) {  // the state before every 16-step chunk (backward pass)
       float* dst = h_ckpt + ((t / 16) * batch * dim + c) * N;
 #pragma unroll
@@ -70,9 +83,17 @@ __global__ void __launch_bounds__(128) sscan_simple_kernel(
 #pragma unroll
     for (int n = 0; n < kNP; ++n) {
       if (n < N) {
-        const float e = EULER ? fmaf(dt, A2[n], 1.f) : ex2(fmaf(dt, A2[n], kEx2ArgShift));
+        const float e = EULER ? fmaf(dt, A2[n], 1.f) : ex2(dt * A2[n]);
         h[n] = fmaf(e, h[n], dtu * to_f32(Bt[n]));
         acc = fmaf(to_f32(Ct[n]), h[n], acc);
+        if constexpr (kAnchor) R[n] *= e;
+      }
+    }
+    if constexpr (kAnchor) {
+      S += dt;
+      if (t % 16 == 15 || t == L - 1) {  // end of a block: its decay from the summed step
+#pragma unroll
+        for (int n = 0; n < kNP; ++n) h[n] = fmaf(exp2_acc(A2[n] * S) - R[n], hs[n], h[n]);
       }
     }
     float yv = fmaf(Dd, uu, acc);
@@ -230,7 +251,18 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
   // Decay factor of one step: 2^(dt * A log2e) on the SFU (zero-order hold), or 1 + dt * A (first
   // order). A2 holds A log2e or A accordingly; kArg is the addend of the FMA.
   constexpr float kScaleA = EULER ? 1.f : kLog2e;
-  constexpr float kArg = EULER ? 1.f : kEx2ArgShift;
+  constexpr float kArg = EULER ? 1.f : 0.f;
+  // fp32 io with the zero-order hold re-anchors the decay every 16 steps: the state's component
+  // carried in from before a 16-step window is decayed by 2^(A log2e S), S the window's summed
+  // step, computed accurately on the FMA pipe (exp2_acc2), instead of by the product R of the
+  // window's per-step SFU factors: h_end += (2^(A log2e S) - R) h_start. The SFU's rounding (on
+  // this hardware a third of an ulp low on average for the scan's arguments) then compounds over
+  // at most 16 steps, not over the state's whole memory (hundreds to thousands of steps for
+  // small dt). It costs one FMUL per update (R) and one accurate exponential per state and
+  // window. bf16 io keeps the plain SFU product: its tolerance admits that rounding.
+  constexpr bool kAnchor = std::is_same<IO, float>::value && !EULER;
+  constexpr int kAnchorW = 16;  // re-anchoring window, steps (TC is a multiple of it)
+  static_assert(TC % kAnchorW == 0, "chunk must hold whole re-anchoring windows");
   auto decay = [](float2 arg) -> float2 {
     if constexpr (EULER)
       return arg;
@@ -387,7 +419,10 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         const float* a = p.agg + (uj * 32 + lane) * (2 * K);
 #pragma unroll
         for (int r = 0; r < KP; ++r) {  // acc <- acc o agg_j: agg_j's end state decays over acc
-          if constexpr (!EULER) accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+          if constexpr (kAnchor)
+            accP[r] = exp2_acc2(__fmul2_rn(A2[r], f2(acc_sd, acc_sd)));
+          else if constexpr (!EULER)
+            accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
           accH[r] = __ffma2_rn(accP[r], f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
           if constexpr (EULER)
             accP[r] = __fmul2_rn(accP[r], f2(__ldcg(a + K + 2 * r), __ldcg(a + K + 2 * r + 1)));
@@ -396,7 +431,10 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       }
 #pragma unroll
       for (int r = 0; r < KP; ++r) {
-        if constexpr (!EULER) accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
+        if constexpr (kAnchor)
+          accP[r] = exp2_acc2(__fmul2_rn(A2[r], f2(acc_sd, acc_sd)));
+        else if constexpr (!EULER)
+          accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
         h[r] = __ffma2_rn(accP[r], hz[r], accH[r]);
       }
     }
@@ -436,8 +474,8 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       // Prologue: dt = softplus(delta + bias) and dt * u, two steps at a time in f32x2, kept as
       // duplicated pairs {v, v} for all TC steps, ready as packed-FMA operands. With one or two
       // lanes per channel every lane computes all TC steps (recomputing is cheaper than trading
-      // them); with four, lane g computes only its own steps t = g + 4 k and the four lanes
-      // trade them with shuffles. Steps past the end of the sequence get dt = 0, an identity
+      // them); with four, lane g computes only its own steps t = g + 4 k and publishes them in
+      // a per-warp table the four lanes read. Steps past the end of the sequence get dt = 0, an identity
       // update. uo keeps u of this lane's own output steps for the skip term.
       constexpr int OWN = TC / G;
       constexpr bool kShare = G == 4;
@@ -459,6 +497,52 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         own_u[k] = u2.x;
         own_u[k + 1] = u2.y;
       }
+      // The summed step of every re-anchoring window (kAnchorW steps): each lane sums the
+      // window's steps it computed; with four lanes per channel the partial sums are combined by
+      // two exchanges, which give all four lanes the same value (the additions see the same
+      // operands in every lane).
+      constexpr int NWIN = kAnchor ? TC / kAnchorW : 1;
+      float S_win[NWIN];
+#pragma unroll
+      for (int wi = 0; wi < NWIN; ++wi) S_win[wi] = 0.f;
+      if constexpr (kAnchor) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          const int t = kShare ? g + G * k : k;  // the step own_dt[k] belongs to
+          S_win[t / kAnchorW] += own_dt[k];
+        }
+        if constexpr (kShare) {
+#pragma unroll
+          for (int wi = 0; wi < NWIN; ++wi) {
+            S_win[wi] += __shfl_xor_sync(0xffffffffu, S_win[wi], 1);
+            S_win[wi] += __shfl_xor_sync(0xffffffffu, S_win[wi], 2);
+          }
+        }
+      }
+      // Window-start state and product of the window's factors (re-anchoring).
+      float2 hs[kAnchor ? KP : 1], Rp[kAnchor ? KP : 1];
+      auto open_window = [&]() {
+#pragma unroll
+        for (int r = 0; r < (kAnchor ? KP : 1); ++r) {
+          hs[r] = h[r];
+          Rp[r] = f2(1.f, 1.f);
+        }
+      };
+      open_window();
+      // After step t: at the end of a window, decay its start state by the accurate factor.
+      auto reanchor = [&](int t) {
+        if constexpr (kAnchor) {
+          if (t % kAnchorW == kAnchorW - 1) {
+            const float S = S_win[t / kAnchorW];
+#pragma unroll
+            for (int r = 0; r < KP; ++r) {
+              const float2 P = exp2_acc2(__fmul2_rn(A2[r], f2(S, S)));
+              h[r] = __ffma2_rn(__fadd2_rn(P, __fmul2_rn(Rp[r], f2(-1.f, -1.f))), hs[r], h[r]);
+            }
+            open_window();
+          }
+        }
+      };
       // With four lanes per channel dt and dt u stay scalars (scalar FMAs cost the same
       // dispatch cycles as paired ones and need no duplicated pairs, which leaves registers for
       // longer chunks); otherwise they are duplicated pairs for the packed FMAs.
@@ -529,8 +613,10 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
               const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
               h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
               if constexpr (EULER) Pr[r] = __fmul2_rn(Pr[r], dA);
+              if constexpr (kAnchor) Rp[r] = __fmul2_rn(Rp[r], dA);
             }
           }
+          reanchor(t);
         }
         release_stage(s, q);
         const float yk = csum - sd_c;  // Kahan step
@@ -561,9 +647,11 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
             h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
             acc = __ffma2_rn(cc, h[r], acc);
+            if constexpr (kAnchor) Rp[r] = __fmul2_rn(Rp[r], dA);
           }
         }
         ys[t] = acc.x + acc.y;
+        reanchor(t);
       }
 
       // Epilogue on this lane's own steps, two at a time: (readout + D u) * SiLU(z) into the
@@ -700,16 +788,6 @@ bool make_map(CUtensorMap* m, const void* ptr, Io io, uint64_t d0, uint64_t d1, 
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int env_int(const char* name) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : 0;
-}
-
-int env_int_or(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : dflt;
-}
-
 constexpr int kLaneTC = 16;
 constexpr int64_t kSplitBelowWarps = 300;  // fewer warps than this: split the sequence
 
@@ -794,7 +872,7 @@ cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Works
 // Common launch parameters; segments: time segments requested (0: automatic, for `units_per_seg`
 // warp units of state).
 LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64_t units_per_seg,
-                       int TC = kLaneTC) {
+                       int skip_publish, int TC = kLaneTC) {
   LaneParams p;
   p.A = a.A;
   p.D = a.D;
@@ -823,14 +901,15 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
   p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
   p.n_seg = (p.n_chunks + p.seg_chunks - 1) / p.seg_chunks;  // no empty segments
-  p.skip_publish = env_int_or("SSCAN_TEST_SKIP_PUBLISH", -1);
+  p.skip_publish = skip_publish;
   p.ticket = p.flags = nullptr;
   p.agg = nullptr;
   return p;
 }
 
 template <typename IO, int G, int TC, bool EULER>
-cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments) {
+cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments,
+                              int skip_publish) {
   constexpr int CPW = 32 / G;
   constexpr int K = kNP / G;
   const int W = threads / 32;
@@ -847,7 +926,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
   const int64_t n_cg = (a.dim + CH - 1) / CH;
   const int64_t warps_per_seg = a.batch * n_cg * W;
-  LaneParams p = base_params(a, CH, stages, segments, warps_per_seg, TC);
+  LaneParams p = base_params(a, CH, stages, segments, warps_per_seg, skip_publish, TC);
 
   Workspace w;
   cudaError_t e = prepare_workspace(a, p.n_seg > 1 ? size_t(p.n_seg) * warps_per_seg : 0, K, &w);
@@ -882,17 +961,17 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
 // few state updates per step), else 16; always 16 when the backward pass wants checkpoints.
 template <typename IO, bool EULER>
 cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int segments,
-                          int chunk) {
-  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, stages, segments);
-  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, stages, segments);
+                          int chunk, int skip) {
+  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, stages, segments, skip);
+  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, stages, segments, skip);
   const bool long_chunks = !a.h_ckpt && chunk != 16 && threads <= 128;
-  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, stages, segments)
-                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, stages, segments);
+  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, stages, segments, skip)
+                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, stages, segments, skip);
 }
 
 }  // namespace
 
-cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
+cudaError_t launch_lane(const FwdArgs& a, const Tuning& tune) {
   // Layout from the number of channels (batch x dim), measured on B300: one lane per channel
   // (16 states per lane, 256-thread CTAs) from about 24k channels up; two lanes (128 threads)
   // from about 16k; four lanes (64 threads, 32-step chunks) below that. When the sequence will be split into
@@ -908,23 +987,12 @@ cudaError_t launch_lane(const FwdArgs& a, const TmaTuning& tune) {
   const int es = a.io == Io::F32 ? 4 : 2;
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
-  const int st = tune.stages, sg = tune.segments, tc = tune.chunk;
-  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg, tc)
-                                      : launch_lane_g<float, false>(a, G, threads, st, sg, tc);
+  const int st = tune.stages, sg = tune.segments, tc = tune.chunk, sk = tune.skip_publish;
+  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg, tc, sk)
+                                      : launch_lane_g<float, false>(a, G, threads, st, sg, tc, sk);
   using bf = __nv_bfloat16;
-  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg, tc)
-                 : launch_lane_g<bf, false>(a, G, threads, st, sg, tc);
-}
-
-TmaTuning tuning_from_env() {
-  TmaTuning t;
-  t.states_per_lane = env_int("SSCAN_K");
-  t.segments = env_int("SSCAN_SEGMENTS");
-  t.threads = env_int("SSCAN_THREADS");
-  t.stages = env_int("SSCAN_STAGES");
-  t.chunk = env_int("SSCAN_TC");
-
-  return t;
+  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg, tc, sk)
+                 : launch_lane_g<bf, false>(a, G, threads, st, sg, tc, sk);
 }
 
 bool tma_path_ok(const FwdArgs& a) {
@@ -937,7 +1005,13 @@ bool tma_path_ok(const FwdArgs& a) {
   return get_encode() != nullptr;
 }
 
-cudaError_t launch_tma(const FwdArgs& a, const TmaTuning& tune) { return launch_lane(a, tune); }
+cudaError_t launch_tma(const FwdArgs& a, const Tuning& tune) { return launch_lane(a, tune); }
+
+cudaError_t launch_forward(const FwdArgs& a) {
+  const Tuning tune = current_tuning();
+  if (!tune.force_plain && tma_path_ok(a)) return launch_tma(a, tune);
+  return launch_simple(a);
+}
 
 namespace {
 
@@ -991,7 +1065,7 @@ __global__ void __launch_bounds__(256) sscan_step_kernel(
     const float4 av = load4(A + d * N + 4 * q);
     const float4 bv = load4(Bm + b * N + 4 * q), cv = load4(Cm + b * N + 4 * q);
     auto fac = [&](float a) {
-      return EULER ? fmaf(dt, a, 1.f) : ex2(fmaf(dt, a * kLog2e, kEx2ArgShift));
+      return EULER ? fmaf(dt, a, 1.f) : ex2(dt * (a * kLog2e));
     };
     float4 hn;
     hn.x = fmaf(fac(av.x), hv.x, dtu * bv.x);
@@ -1010,7 +1084,7 @@ __global__ void __launch_bounds__(256) sscan_step_kernel(
       const int n = 4 * q + i;
       if (n < N) {
         const float e = EULER ? fmaf(dt, A[d * N + n], 1.f)
-                              : ex2(fmaf(dt, A[d * N + n] * kLog2e, kEx2ArgShift));
+                              : ex2(dt * (A[d * N + n] * kLog2e));
         const float hn = fmaf(e, h[c * N + n], dtu * to_f32(Bm[b * N + n]));
         h[c * N + n] = hn;
         part = fmaf(to_f32(Cm[b * N + n]), hn, part);
@@ -1050,6 +1124,19 @@ cudaError_t launch_simple(const FwdArgs& a) {
     return a.euler ? launch_simple_typed<float, true>(a) : launch_simple_typed<float, false>(a);
   using bf = __nv_bfloat16;
   return a.euler ? launch_simple_typed<bf, true>(a) : launch_simple_typed<bf, false>(a);
+}
+
+__global__ void __launch_bounds__(256) exp2_accurate_kernel(const float* __restrict__ x,
+                                                            float* __restrict__ y, int64_t n) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x)
+    y[i] = exp2_acc(x[i]);
+}
+
+cudaError_t launch_exp2_accurate(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 148 * 16);
+  exp2_accurate_kernel<<<unsigned(blocks), 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_step(const FwdArgs& a) {

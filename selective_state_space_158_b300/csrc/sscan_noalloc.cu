@@ -88,11 +88,7 @@ extern "C" sscan_status_t sscan_fwd_noalloc(const void* u, const void* delta, co
   a.scratch = base + kStatusBytes;
   a.scratch_bytes = kScratchBytes - kStatusBytes;
   a.scratch_short = &short_scratch;
-  cudaError_t e;
-  if (sscan::tma_path_ok(a))
-    e = sscan::launch_tma(a, sscan::tuning_from_env());
-  else
-    e = sscan::launch_simple(a);  // needs no scratch
+  const cudaError_t e = sscan::launch_forward(a);  // the plain-load kernel needs no scratch
   if (short_scratch) return SSCAN_ERR_SCRATCH_TOO_SMALL;
   return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
