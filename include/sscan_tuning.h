@@ -29,6 +29,8 @@ typedef struct {
   int force_plain;       /* forward: 1 = always the plain-load kernel (0: TMA path when possible) */
   int bwd_segments;      /* backward: time segments (0: auto) */
   int conv_plain;        /* Conv1d: 1 = always the register-window kernel (0: TMA when possible) */
+  int ctas_per_sm;       /* forward: at most this many thread blocks resident per SM, 1..32
+                            (enforced through each block's shared-memory reservation; 0: auto) */
   int test_skip_publish; /* fault injection: the time segment with this index never publishes
                             its chunk-carry summary, so that its successors' bounded waits run
                             out and report SSCAN_ERR_CARRY_TIMEOUT (-1: off) */

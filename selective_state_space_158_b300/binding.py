@@ -45,7 +45,8 @@ class Tuning(ctypes.Structure):
     _fields_ = [("states_per_lane", ctypes.c_int), ("segments", ctypes.c_int),
                 ("threads", ctypes.c_int), ("stages", ctypes.c_int), ("chunk", ctypes.c_int),
                 ("force_plain", ctypes.c_int), ("bwd_segments", ctypes.c_int),
-                ("conv_plain", ctypes.c_int), ("test_skip_publish", ctypes.c_int)]
+                ("conv_plain", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("test_skip_publish", ctypes.c_int)]
 
 
 _TUNING_P = ctypes.POINTER(Tuning)

@@ -106,7 +106,8 @@ sscan_status_t sscan_set_tuning(const sscan_tuning_t* t) {
     if ((k != 0 && k != 4 && k != 8 && k != 16) || t->segments < 0 || t->threads < 0 ||
         t->threads > 256 || t->threads % 32 != 0 || t->stages < 0 || t->stages > 8 ||
         t->stages == 1 || (t->chunk != 0 && t->chunk != 16 && t->chunk != 32) ||
-        t->bwd_segments < 0 || t->test_skip_publish < -1)
+        t->bwd_segments < 0 || t->test_skip_publish < -1 || t->ctas_per_sm < 0 ||
+        t->ctas_per_sm > 32)
       return SSCAN_ERR_INVALID_ARG;
     n.states_per_lane = k;
     n.segments = t->segments;
@@ -116,6 +117,7 @@ sscan_status_t sscan_set_tuning(const sscan_tuning_t* t) {
     n.force_plain = t->force_plain != 0;
     n.bwd_segments = t->bwd_segments;
     n.conv_plain = t->conv_plain != 0;
+    n.ctas_per_sm = t->ctas_per_sm;
     n.skip_publish = t->test_skip_publish;
   }
   std::lock_guard<std::mutex> lk(g_tune_mu);
@@ -141,6 +143,7 @@ sscan_status_t sscan_get_tuning(sscan_tuning_t* t) {
   t->force_plain = c.force_plain;
   t->bwd_segments = c.bwd_segments;
   t->conv_plain = c.conv_plain;
+  t->ctas_per_sm = c.ctas_per_sm;
   t->test_skip_publish = c.skip_publish;
   return SSCAN_OK;
 }

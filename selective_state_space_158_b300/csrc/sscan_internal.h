@@ -49,6 +49,7 @@ struct Tuning {
   int force_plain = 0;        // forward: plain-load kernel only
   int bwd_segments = 0;       // backward: time segments
   int conv_plain = 0;         // Conv1d: register-window kernel only
+  int ctas_per_sm = 0;        // forward: cap on resident CTAs per SM (0: no cap)
   int skip_publish = -1;      // test hook: this segment never publishes its aggregate
 };
 

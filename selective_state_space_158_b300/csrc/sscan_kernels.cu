@@ -120,17 +120,19 @@ __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_
 // Long sequences are split into n_seg time segments run by different CTAs ("chunk carry"). The
 // scan operator (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) is associative ("架构变体：Mamba/SSM",
 // "硬件感知算法": the update can be evaluated as a tree), so a segment is summarised by its
-// aggregate: the end state from a zero start, H, and its summed step SD (its decay factor is
-// 2^(A log2e SD), exact for a product of zero-order-hold factors). A segment CTA
-//   1. runs pass 1 over its steps (no readout) and publishes its aggregate (if it has a
-//      successor);
-//   2. looks back over every predecessor's published aggregate and folds them, nearest first,
-//      into its true start state h_in (a fixed order: the result is deterministic);
+// aggregate: the end state from a zero start, H, and its decay over the segment, 2^(A log2e SD)
+// with SD its summed step (exact for a product of zero-order-hold factors). A segment CTA
+//   1. runs pass 1 over its steps (no readout) to its aggregate (segment 0 from its true start
+//      state h0, so its pass 1 ends on its inclusive prefix);
+//   2. waits for the inclusive prefix of segment s - 1 (its true start state h_in), publishes
+//      its own inclusive prefix 2^(A log2e SD) h_in + H for segment s + 1 (a decoupled
+//      look-back of depth one: each segment folds exactly one aggregate onto its predecessor's
+//      prefix, a fixed association, so the result is deterministic);
 //   3. runs pass 2 from h_in with readout, gate and stores.
-// Aggregates depend on nothing but the segment's own inputs, so no wait forms a chain. CTAs take
-// segment numbers from an atomic ticket in launch order, segment-major, so every CTA they wait
-// on is already resident or finished; every wait is bounded and reports a timeout through the
-// device status word instead of hanging.
+// CTAs take segment numbers from an atomic ticket in launch order, segment-major, so every CTA
+// they wait on is already resident or finished, and a segment's predecessor publishes right
+// after its own pass 1 and wait; every wait is bounded and reports a timeout through the device
+// status word instead of hanging.
 // ================================================================================================
 struct LaneParams {
   const float* A;
@@ -149,8 +151,8 @@ struct LaneParams {
   int seg_chunks;  // chunks per segment
   // chunk-carry workspace (n_seg > 1)
   unsigned int* ticket;  // zero at launch
-  unsigned int* flags;   // [n_seg][batch][n_cg][W] warp units
-  float* agg;            // [unit][lane][2K]: H, then SD (zero-order hold) or P (first order)
+  unsigned int* flags;   // [n_seg][batch][n_cg][W] warp units: inclusive prefix published
+  float* agg;            // [unit][lane][2K]: the segment's inclusive prefix (K states)
   int skip_publish;      // test hook: this segment never publishes (-1: off)
 };
 
@@ -228,16 +230,24 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_shared(unsigned* p, unsigne
   return old;
 }
 
-// Launch bounds: up to 256 threads and 255 registers with one or two lanes per channel; with
-// four there are more warps to keep resident: at most 128 registers with 16-step chunks, and
-// 128-thread CTAs at 170 registers (three per SM) with 32-step chunks.
+// Launch bounds: up to 256 threads and 255 registers with one lane per channel (its 16 states
+// and the chunk's steps need them); with two or four lanes per channel there are more warps to
+// keep resident: 128-thread CTAs at 128 registers (four per SM; 170 and three per SM for fp32
+// io) with two lanes, at most 128
+// registers with four lanes and 16-step chunks, and 128-thread CTAs at 170 registers (three per
+// SM) with four lanes and 32-step chunks.
 template <int G, int TC>
-__host__ __device__ constexpr int lane_max_threads() { return (G == 4 && TC == 32) ? 128 : 256; }
-template <int G, int TC>
-__host__ __device__ constexpr int lane_min_blocks() { return G == 4 ? (TC == 32 ? 3 : 2) : 1; }
+__host__ __device__ constexpr int lane_max_threads() {
+  return ((G == 4 && TC == 32) || G == 2) ? 128 : 256;
+}
+template <typename IO, int G, int TC>
+__host__ __device__ constexpr int lane_min_blocks() {
+  // two lanes, fp32 io: the re-anchoring registers need 170 (three CTAs per SM)
+  return G == 4 ? (TC == 32 ? 3 : 2) : (G == 2 ? (std::is_same<IO, float>::value ? 3 : 4) : 1);
+}
 
 template <typename IO, int G, int TC, bool EULER>
-__global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, TC>())
+__global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO, G, TC>())
     sscan_lane_kernel(
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int W = nthr >> 5, CH = W * CPW;
   const int N = p.N, S = p.stages;
-  const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S, G == 4);
+  const LaneSmem lay(TC, W, CPW, int(sizeof(IO)), S, G >= 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
   unsigned* done = reinterpret_cast<unsigned*>(smem + lay.off_bar + 8 * 8);
   unsigned* s_ticket = done + 8;
@@ -360,9 +370,8 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
   const int cg = ch0 + cl;               // global channel
   const bool live = cg < p.dim;
   float2 A2[KP], h[KP], hz[KP];
-  // The initial state, read once before anything is written (so h0 may alias h_last). It
-  // enters the first pass directly when the sequence is not split, and through the fold of
-  // predecessor aggregates below when it is.
+  // The initial state, read once before anything is written (so h0 may alias h_last). It is
+  // the start state of segment 0 (of the only segment when the sequence is not split).
   const float* h0c = (p.h0 && live) ? p.h0 + (size_t(b) * p.dim + cg) * N : nullptr;
 #pragma unroll
   for (int r = 0; r < KP; ++r) {
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
     A2[r] = f2((live && n < N) ? p.A[size_t(cg) * N + n] * kScaleA : 0.f,
                (live && n + 1 < N) ? p.A[size_t(cg) * N + n + 1] * kScaleA : 0.f);
     hz[r] = f2((h0c && n < N) ? h0c[n] : 0.f, (h0c && n + 1 < N) ? h0c[n + 1] : 0.f);
-    h[r] = p.n_seg == 1 ? hz[r] : f2(0.f, 0.f);
+    h[r] = seg == 0 ? hz[r] : f2(0.f, 0.f);
   }
   float2 Pr[EULER ? KP : 1];  // first order: product of this segment's decay factors (pass 1)
 #pragma unroll
@@ -390,24 +399,24 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
   for (int pass = agg_pass ? 0 : 1; pass < 2 && !timed_out; ++pass) {
     const bool readout = pass == 1;
     if (readout && p.n_seg > 1) {
-      // Start state of this segment: predecessors' aggregates folded from the nearest back to
-      // segment 0 (later o earlier), always in that order, so the result is deterministic;
-      // then the initial state decayed over all of them. (Segment 0 starts from h0 or zero;
-      // pass 1 left its aggregate in h.) accP is the decay accumulated so far: 2^(A2 acc_sd)
-      // for zero-order hold, the running product of the segments' P for first order.
-      float2 accH[KP], accP[KP];
+      // Chunk carry between segments. Segment 0 knows its start state (h0 or zero), so its
+      // first pass ended on its true end state: its inclusive prefix. Segment s > 0 waits for
+      // segment s - 1's inclusive prefix (its start state), and, if it has a successor, folds
+      // its own aggregate onto it and publishes its inclusive prefix:
+      //   incl_s = P_s incl_{s-1} + H_s,   P_s = 2^(A log2e SD_s) (zero-order hold; SD_s the
+      //   segment's summed step) or the product of its factors (first order).
+      // The association is fixed (always one segment onto its predecessor's prefix), so the
+      // result is deterministic, and one wait per segment suffices.
+      float2 start[KP];
+      if (seg == 0) {
 #pragma unroll
-      for (int r = 0; r < KP; ++r) {
-        accH[r] = f2(0.f, 0.f);
-        accP[r] = f2(1.f, 1.f);
-      }
-      float acc_sd = 0.f;
-      for (int j = seg - 1; j >= 0; --j) {
-        const size_t uj = unit - size_t(seg - j) * units_per_seg;
+        for (int r = 0; r < KP; ++r) start[r] = hz[r];
+      } else {
+        const size_t up = unit - units_per_seg;  // the same lanes of segment s - 1
         unsigned f = 0;
         if (lane == 0) {
           for (uint32_t it = 0; it < kLookbackTries; ++it) {
-            f = ld_acquire(p.flags + uj);
+            f = ld_acquire(p.flags + up);
             if (f != 0) break;
             __nanosleep(512);
           }
@@ -415,28 +424,35 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         }
         f = __shfl_sync(0xffffffffu, f, 0);
         __syncwarp();
-        if (f == 0) continue;  // timed out: the status word says so; skip this aggregate
-        const float* a = p.agg + (uj * 32 + lane) * (2 * K);
+        const float* a = p.agg + (up * 32 + lane) * (2 * K);
 #pragma unroll
-        for (int r = 0; r < KP; ++r) {  // acc <- acc o agg_j: agg_j's end state decays over acc
-          if constexpr (kAnchor)
-            accP[r] = exp2_acc2(__fmul2_rn(A2[r], f2(acc_sd, acc_sd)));
-          else if constexpr (!EULER)
-            accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
-          accH[r] = __ffma2_rn(accP[r], f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)), accH[r]);
-          if constexpr (EULER)
-            accP[r] = __fmul2_rn(accP[r], f2(__ldcg(a + K + 2 * r), __ldcg(a + K + 2 * r + 1)));
+        for (int r = 0; r < KP; ++r)  // timed out: zero (the status word says the result is wrong)
+          start[r] = f != 0 ? f2(__ldcg(a + 2 * r), __ldcg(a + 2 * r + 1)) : f2(0.f, 0.f);
+      }
+      if (agg_pass && !timed_out && seg != p.skip_publish) {
+        float* my = p.agg + (unit * 32 + lane) * (2 * K);
+#pragma unroll
+        for (int r = 0; r < KP; ++r) {
+          float2 incl = h[r];  // segment 0: the end state from h0 already
+          if (seg > 0) {
+            float2 P;
+            if constexpr (EULER)
+              P = Pr[r];
+            else if constexpr (kAnchor)
+              P = exp2_acc2(__fmul2_rn(A2[r], f2(sd, sd)));
+            else
+              P = f2(ex2(A2[r].x * sd), ex2(A2[r].y * sd));
+            incl = __ffma2_rn(P, start[r], h[r]);
+          }
+          my[2 * r] = incl.x;
+          my[2 * r + 1] = incl.y;
         }
-        if constexpr (!EULER) acc_sd += __ldcg(a + K);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release(p.flags + unit, kFlagAgg);
       }
 #pragma unroll
-      for (int r = 0; r < KP; ++r) {
-        if constexpr (kAnchor)
-          accP[r] = exp2_acc2(__fmul2_rn(A2[r], f2(acc_sd, acc_sd)));
-        else if constexpr (!EULER)
-          accP[r] = f2(ex2(A2[r].x * acc_sd), ex2(A2[r].y * acc_sd));
-        h[r] = __ffma2_rn(accP[r], hz[r], accH[r]);
-      }
+      for (int r = 0; r < KP; ++r) h[r] = start[r];
     }
     for (int ci = 0; ci < nch; ++ci, ++q, s = (s + 1 == S) ? 0 : s + 1, phase ^= (s == 0)) {
       const int c = c_begin + ci;
@@ -471,14 +487,14 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       const float* Bs = reinterpret_cast<const float*>(stage_ptr(s, 3));
       const float* Cs = reinterpret_cast<const float*>(stage_ptr(s, 4));
 
-      // Prologue: dt = softplus(delta + bias) and dt * u, two steps at a time in f32x2, kept as
-      // duplicated pairs {v, v} for all TC steps, ready as packed-FMA operands. With one or two
-      // lanes per channel every lane computes all TC steps (recomputing is cheaper than trading
-      // them); with four, lane g computes only its own steps t = g + 4 k and publishes them in
-      // a per-warp table the four lanes read. Steps past the end of the sequence get dt = 0, an identity
-      // update. uo keeps u of this lane's own output steps for the skip term.
+      // Prologue: dt = softplus(delta + bias) and dt * u, two steps at a time in f32x2. With one
+      // lane per channel the lane computes all TC steps; with G = 2 or 4 lanes, lane g computes
+      // only its own steps t = g + G k and publishes them in a per-warp table that the channel's
+      // lanes read. Steps past the end of the sequence get dt = 0, an identity update. uo keeps
+      // u of this lane's own output steps for the skip term.
       constexpr int OWN = TC / G;
-      constexpr bool kShare = G == 4;
+      constexpr bool kShare = G >= 2;        // lanes of a channel split the prologue
+      constexpr bool kScalarArgs = G == 4;   // dt, dt u kept as scalars (registers)
       constexpr int NP = kShare ? OWN : TC;  // steps this lane computes
       float own_dt[NP], own_du[NP], own_u[NP], uo[OWN];
 #pragma unroll
@@ -498,8 +514,8 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         own_u[k + 1] = u2.y;
       }
       // The summed step of every re-anchoring window (kAnchorW steps): each lane sums the
-      // window's steps it computed; with four lanes per channel the partial sums are combined by
-      // two exchanges, which give all four lanes the same value (the additions see the same
+      // window's steps it computed; with G lanes per channel the partial sums are combined by
+      // log2 G exchanges, which give all G lanes the same value (the additions see the same
       // operands in every lane).
       constexpr int NWIN = kAnchor ? TC / kAnchorW : 1;
       float S_win[NWIN];
@@ -514,8 +530,8 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         if constexpr (kShare) {
 #pragma unroll
           for (int wi = 0; wi < NWIN; ++wi) {
-            S_win[wi] += __shfl_xor_sync(0xffffffffu, S_win[wi], 1);
-            S_win[wi] += __shfl_xor_sync(0xffffffffu, S_win[wi], 2);
+#pragma unroll
+            for (int m = 1; m < G; m <<= 1) S_win[wi] += __shfl_xor_sync(0xffffffffu, S_win[wi], m);
           }
         }
       }
@@ -543,50 +559,51 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
           }
         }
       };
-      // With four lanes per channel dt and dt u stay scalars (scalar FMAs cost the same
-      // dispatch cycles as paired ones and need no duplicated pairs, which leaves registers for
-      // longer chunks); otherwise they are duplicated pairs for the packed FMAs.
-      constexpr int NPAIR = kShare ? 1 : TC;
-      float2 dtp[NPAIR], dtup[NPAIR];
-      float dts[kShare ? TC : 1], dus[kShare ? TC : 1];
-      if constexpr (kShare) {  // lane g publishes its own steps t = g + G k in the warp's table
+      // With four lanes per channel dt and dt u stay scalars (scalar FMAs need no duplicated
+      // pairs, which leaves registers for longer chunks); otherwise they are duplicated pairs
+      // {v, v} for the packed FMAs.
+      // G = 1: the lane's own dt, dt u as duplicated pairs {v, v} for the packed FMAs. G > 1:
+      // lane g publishes its own steps t = g + G k in the warp's table, and every lane reads
+      // each step's (dt, dt u) from it when the step comes (no register copy of the chunk).
+      float2 dtp[kShare ? 1 : TC], dtup[kShare ? 1 : TC];
+      const float2* tabr = nullptr;
+      if constexpr (kShare) {
         float2* tab = reinterpret_cast<float2*>(smem + lay.off_tab + size_t(warp) * lay.tab_warp);
         __syncwarp();  // every lane has read the previous chunk's entries
 #pragma unroll
         for (int k = 0; k < OWN; ++k) tab[(g + G * k) * CPW + lane / G] = f2(own_dt[k], own_du[k]);
         __syncwarp();
-#pragma unroll
-        for (int t = 0; t < TC; ++t) {
-          const float2 v = tab[t * CPW + lane / G];
-          dts[t] = v.x;
-          dus[t] = v.y;
-        }
-      }
-      if constexpr (!kShare) {
+        tabr = tab + lane / G;
+      } else {
 #pragma unroll
         for (int t = 0; t < TC; ++t) {
           dtp[t] = f2(own_dt[t], own_dt[t]);
           dtup[t] = f2(own_du[t], own_du[t]);
         }
       }
-      // dA argument and input term of state pair r at step t.
-      auto arg_at = [&](int t, int r) -> float2 {
+      // (dt, dt u) of step t.
+      auto step_at = [&](int t) -> float2 {
         if constexpr (kShare)
-          return f2(fmaf(dts[t], A2[r].x, kArg), fmaf(dts[t], A2[r].y, kArg));
+          return tabr[t * CPW];
+        else
+          return f2(dtp[t].x, dtup[t].x);
+      };
+      // dA argument and input term of state pair r at step t, given the step's (dt, dt u).
+      auto arg_at = [&](float2 v, int t, int r) -> float2 {
+        if constexpr (kScalarArgs)
+          return f2(fmaf(v.x, A2[r].x, kArg), fmaf(v.x, A2[r].y, kArg));
+        else if constexpr (kShare)
+          return __ffma2_rn(f2(v.x, v.x), A2[r], f2(kArg, kArg));
         else
           return __ffma2_rn(dtp[t], A2[r], f2(kArg, kArg));
       };
-      auto in_at = [&](int t, float2 bb) -> float2 {
-        if constexpr (kShare)
-          return f2(dus[t] * bb.x, dus[t] * bb.y);
+      auto in_at = [&](float2 v, int t, float2 bb) -> float2 {
+        if constexpr (kScalarArgs)
+          return f2(v.y * bb.x, v.y * bb.y);
+        else if constexpr (kShare)
+          return __fmul2_rn(f2(v.y, v.y), bb);
         else
           return __fmul2_rn(dtup[t], bb);
-      };
-      auto dt_at = [&](int t) -> float {
-        if constexpr (kShare)
-          return dts[t];
-        else
-          return dtp[t].x;
       };
 #pragma unroll
       for (int k = 0; k < OWN; ++k) {
@@ -602,16 +619,17 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
 #pragma unroll
         for (int t = 0; t < TC; ++t) {
           const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
-          csum += dt_at(t);
+          const float2 sv = step_at(t);
+          csum += sv.x;
 #pragma unroll
           for (int qq = 0; qq < K / 4; ++qq) {
             const float4 bq = Bq[qq];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int r = 2 * qq + j;
-              const float2 dA = decay(arg_at(t, r));
+              const float2 dA = decay(arg_at(sv, t, r));
               const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
-              h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
+              h[r] = __ffma2_rn(dA, h[r], in_at(sv, t, bb));
               if constexpr (EULER) Pr[r] = __fmul2_rn(Pr[r], dA);
               if constexpr (kAnchor) Rp[r] = __fmul2_rn(Rp[r], dA);
             }
@@ -633,6 +651,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
       for (int t = 0; t < TC; ++t) {
         const float4* Bq = reinterpret_cast<const float4*>(Bs + t * kNP + n0);
         const float4* Cq = reinterpret_cast<const float4*>(Cs + t * kNP + n0);
+        const float2 sv = step_at(t);
         // One chain of packed FMAs per step for the readout: the steps of the unrolled chunk
         // are independent, so a longer chain costs no stall and saves the adds of partial sums.
         float2 acc = f2(0.f, 0.f);
@@ -642,10 +661,10 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int r = 2 * qq + j;
-            const float2 dA = decay(arg_at(t, r));
+            const float2 dA = decay(arg_at(sv, t, r));
             const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
             const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
-            h[r] = __ffma2_rn(dA, h[r], in_at(t, bb));
+            h[r] = __ffma2_rn(dA, h[r], in_at(sv, t, bb));
             acc = __ffma2_rn(cc, h[r], acc);
             if constexpr (kAnchor) Rp[r] = __fmul2_rn(Rp[r], dA);
           }
@@ -678,23 +697,6 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<G, 
         tma_store_commit();
       }
       ++ystores;
-    }
-    if (pass == 0 && !timed_out && seg != p.skip_publish) {
-      // Publish this segment's aggregate: end state from a zero start, and its summed step.
-      float* my_agg = p.agg + (unit * 32 + lane) * (2 * K);
-#pragma unroll
-      for (int r = 0; r < KP; ++r) {
-        my_agg[2 * r] = h[r].x;
-        my_agg[2 * r + 1] = h[r].y;
-        if constexpr (EULER) {
-          my_agg[K + 2 * r] = Pr[r].x;
-          my_agg[K + 2 * r + 1] = Pr[r].y;
-        }
-      }
-      if constexpr (!EULER) my_agg[K] = sd;
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) st_release(p.flags + unit, kFlagAgg);
     }
   }
 
@@ -891,12 +893,14 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   p.n_cg = int((a.dim + CH - 1) / CH);
   p.stages = stages;
   // Chunk carry: split the sequence when too few warps would run otherwise (about 2 per SM),
-  // into enough segments for about 40 warps per SM (measured best on B300 for a long sequence).
+  // into enough segments for about 256 warps per SM in total, i.e. many short waves of resident
+  // CTAs: measured on B300 for the long sequence (batch 1, L 2^20, D 1536, two lanes per
+  // channel), 62 segments 12.6 ms, 123 11.6 ms, 246 11.4 ms, 492 11.25 ms, 740 11.2 ms.
   int n_seg = segments;
   if (n_seg <= 0) {
     n_seg = 1;
     if (units_per_seg < kSplitBelowWarps)
-      n_seg = int((148 * 40 + units_per_seg - 1) / units_per_seg);
+      n_seg = int((148 * 256 + units_per_seg - 1) / units_per_seg);
   }
   n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
   p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
@@ -908,8 +912,10 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
 }
 
 template <typename IO, int G, int TC, bool EULER>
-cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int segments,
-                              int skip_publish) {
+cudaError_t launch_lane_typed(const FwdArgs& a, int threads, const Tuning& tune) {
+  threads = std::min(threads, lane_max_threads<G, TC>());  // the kernel's launch bound
+  int stages = tune.stages;
+  const int segments = tune.segments, skip_publish = tune.skip_publish;
   constexpr int CPW = 32 / G;
   constexpr int K = kNP / G;
   const int W = threads / 32;
@@ -919,11 +925,17 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
   // SM), three otherwise.
   if (stages < 2 || stages > 8) stages = (G == 4 && TC == 32) ? 2 : 3;
   while (stages > 2 &&
-         LaneSmem(TC, W, CPW, es, stages, G == 4).total + 128 > size_t(227) * 1024)
+         LaneSmem(TC, W, CPW, es, stages, G >= 2).total + 128 > size_t(227) * 1024)
     --stages;
-  const LaneSmem lay(TC, W, CPW, es, stages, G == 4);
-  const size_t smem_bytes = lay.total + 128;
+  const LaneSmem lay(TC, W, CPW, es, stages, G >= 2);
+  size_t smem_bytes = lay.total + 128;
   if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
+  if (tune.ctas_per_sm > 0) {
+    // At most ctas_per_sm resident CTAs per SM: reserve enough shared memory that one more does
+    // not fit (228 KB per SM, 1 KB of it reserved per CTA by the system).
+    const size_t cap = size_t(228) * 1024 / size_t(tune.ctas_per_sm + 1) - 1024 + 16;
+    smem_bytes = std::min(std::max(smem_bytes, cap), size_t(227) * 1024);
+  }
   const int64_t n_cg = (a.dim + CH - 1) / CH;
   const int64_t warps_per_seg = a.batch * n_cg * W;
   LaneParams p = base_params(a, CH, stages, segments, warps_per_seg, skip_publish, TC);
@@ -960,13 +972,12 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, int stages, int seg
 // Chunk length: 32 steps with four lanes per channel (their per-chunk fixed cost is spread over
 // few state updates per step), else 16; always 16 when the backward pass wants checkpoints.
 template <typename IO, bool EULER>
-cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int segments,
-                          int chunk, int skip) {
-  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, stages, segments, skip);
-  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, stages, segments, skip);
-  const bool long_chunks = !a.h_ckpt && chunk != 16 && threads <= 128;
-  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, stages, segments, skip)
-                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, stages, segments, skip);
+cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, const Tuning& tune) {
+  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, tune);
+  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, tune);
+  const bool long_chunks = !a.h_ckpt && tune.chunk != 16 && threads <= 128;
+  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, tune)
+                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, tune);
 }
 
 }  // namespace
@@ -974,25 +985,25 @@ cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, int stages, int 
 cudaError_t launch_lane(const FwdArgs& a, const Tuning& tune) {
   // Layout from the number of channels (batch x dim), measured on B300: one lane per channel
   // (16 states per lane, 256-thread CTAs) from about 24k channels up; two lanes (128 threads)
-  // from about 16k; four lanes (64 threads, 32-step chunks) below that. When the sequence will be split into
-  // time segments anyway (too few warps even with four lanes), one lane per channel again.
+  // from about 16k; four lanes (64 threads, 32-step chunks) below that. When the sequence will
+  // be split into time segments anyway (too few warps even with four lanes), two lanes per
+  // channel.
   const int64_t chans = a.batch * a.dim;
   int G = tune.states_per_lane ? kNP / tune.states_per_lane : 0;
   if (G == 0) {
     G = chans >= 24576 ? 1 : (chans >= 16384 ? 2 : 4);
-    if (chans * 4 / 32 < kSplitBelowWarps) G = 1;
+    if (chans * 4 / 32 < kSplitBelowWarps) G = 2;
   }
   const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
   if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
   if (((32 / G) * es) % 16) return cudaErrorInvalidValue;
-  const int st = tune.stages, sg = tune.segments, tc = tune.chunk, sk = tune.skip_publish;
-  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, st, sg, tc, sk)
-                                      : launch_lane_g<float, false>(a, G, threads, st, sg, tc, sk);
+  if (a.io == Io::F32) return a.euler ? launch_lane_g<float, true>(a, G, threads, tune)
+                                      : launch_lane_g<float, false>(a, G, threads, tune);
   using bf = __nv_bfloat16;
-  return a.euler ? launch_lane_g<bf, true>(a, G, threads, st, sg, tc, sk)
-                 : launch_lane_g<bf, false>(a, G, threads, st, sg, tc, sk);
+  return a.euler ? launch_lane_g<bf, true>(a, G, threads, tune)
+                 : launch_lane_g<bf, false>(a, G, threads, tune);
 }
 
 bool tma_path_ok(const FwdArgs& a) {
