@@ -28,18 +28,31 @@ __device__ __forceinline__ float ex2(float x) {
 // ---- paired (f32x2) forms used per (step, channel pair) ------------------------------------
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
-// log1p(s)/s on [0, 1]: degree-9 polynomial from Chebyshev interpolation in double precision,
-// re-expanded in powers of s and rounded to fp32 (csrc/gen_softplus_poly.py regenerates it).
-// s * p(s) matches log1p(s) to 1.6e-7 relative in fp32 on the whole interval.
+// log1p(s)/s on [0, 1] by a polynomial from Chebyshev interpolation in double precision,
+// re-expanded in powers of s and rounded to fp32 (csrc/gen_softplus_poly.py regenerates both):
+// degree 9, s * p(s) within 1.6e-7 relative of log1p(s) in fp32 on the whole interval (the fp32
+// io path); degree 6, within 1.5e-6 (bf16 io, where it is far inside the tolerance and saves
+// three FMAs per step).
+template <bool kDeg6 = false>
 __device__ __forceinline__ float2 log1p_unit2(float2 s) {
-  constexpr float c[10] = {1.000000000e+00f, -4.999989271e-01f, 3.332971036e-01f,
-                           -2.495161593e-01f, 1.966327429e-01f, -1.526966691e-01f,
-                           1.054362357e-01f, -5.637361482e-02f, 1.954252832e-02f,
-                           -3.176057013e-03f};
-  float2 acc = f2(c[9], c[9]);
+  if constexpr (kDeg6) {
+    constexpr float c[7] = {9.999985695e-01f, -4.998590052e-01f, 3.309752643e-01f,
+                            -2.345452011e-01f, 1.482941359e-01f, -6.559030712e-02f,
+                            1.387448423e-02f};
+    float2 acc = f2(c[6], c[6]);
 #pragma unroll
-  for (int i = 8; i >= 0; --i) acc = __ffma2_rn(acc, s, f2(c[i], c[i]));
-  return __fmul2_rn(s, acc);
+    for (int i = 5; i >= 0; --i) acc = __ffma2_rn(acc, s, f2(c[i], c[i]));
+    return __fmul2_rn(s, acc);
+  } else {
+    constexpr float c[10] = {1.000000000e+00f, -4.999989271e-01f, 3.332971036e-01f,
+                             -2.495161593e-01f, 1.966327429e-01f, -1.526966691e-01f,
+                             1.054362357e-01f, -5.637361482e-02f, 1.954252832e-02f,
+                             -3.176057013e-03f};
+    float2 acc = f2(c[9], c[9]);
+#pragma unroll
+    for (int i = 8; i >= 0; --i) acc = __ffma2_rn(acc, s, f2(c[i], c[i]));
+    return __fmul2_rn(s, acc);
+  }
 }
 
 // 2^x on the FMA pipe, accurate to about one ulp and unbiased (the fp32 path's decay over a
@@ -75,10 +88,11 @@ __device__ __forceinline__ float2 exp2_acc2(float2 x) {
 __device__ __forceinline__ float exp2_acc(float x) { return exp2_acc2(f2(x, 0.f)).x; }
 
 // softplus on a pair: max(x, 0) + log1p(exp(-|x|)); one SFU exponential per element.
+template <bool kDeg6 = false>
 __device__ __forceinline__ float2 softplus2(float2 x) {
   const float2 e = __fmul2_rn(f2(-fabsf(x.x), -fabsf(x.y)), f2(kLog2e, kLog2e));
   const float2 s = f2(ex2(e.x), ex2(e.y));
-  return __fadd2_rn(f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2(s));
+  return __fadd2_rn(f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2<kDeg6>(s));
 }
 
 // softplus(x) = log(1 + e^x), the positivity map of the step ("Mamba：选择性状态空间模型入门教程",

@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
   // small dt). It costs one FMUL per update (R) and one accurate exponential per state and
   // window. bf16 io keeps the plain SFU product: its tolerance admits that rounding.
   constexpr bool kAnchor = std::is_same<IO, float>::value && !EULER;
+  constexpr bool kBf16Io = !std::is_same<IO, float>::value;  // shorter softplus polynomial
   constexpr int kAnchorW = 16;  // re-anchoring window, steps (TC is a multiple of it)
   static_assert(TC % kAnchorW == 0, "chunk must hold whole re-anchoring windows");
   auto decay = [](float2 arg) -> float2 {
@@ -497,22 +498,28 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
       constexpr bool kScalarArgs = G == 4;   // dt, dt u kept as scalars (registers)
       constexpr int NP = kShare ? OWN : TC;  // steps this lane computes
       float own_dt[NP], own_du[NP], own_u[NP], uo[OWN];
+      auto prologue = [&](auto with_softplus) {
 #pragma unroll
-      for (int k = 0; k < NP; k += 2) {
-        const int ta = kShare ? g + G * k : k, tb = kShare ? ta + G : k + 1;
-        const float2 u2 = f2(to_f32(u_s[ta * CH]), to_f32(u_s[tb * CH]));
-        float2 d2 = __fadd2_rn(f2(to_f32(dl_s[ta * CH]), to_f32(dl_s[tb * CH])),
-                               f2(bias_c, bias_c));
-        if (p.softplus) d2 = softplus2(d2);
-        d2 = f2(ta < t_valid ? d2.x : 0.f, tb < t_valid ? d2.y : 0.f);
-        const float2 du = __fmul2_rn(d2, u2);
-        own_dt[k] = d2.x;
-        own_dt[k + 1] = d2.y;
-        own_du[k] = du.x;
-        own_du[k + 1] = du.y;
-        own_u[k] = u2.x;
-        own_u[k + 1] = u2.y;
-      }
+        for (int k = 0; k < NP; k += 2) {
+          const int ta = kShare ? g + G * k : k, tb = kShare ? ta + G : k + 1;
+          const float2 u2 = f2(to_f32(u_s[ta * CH]), to_f32(u_s[tb * CH]));
+          float2 d2 = __fadd2_rn(f2(to_f32(dl_s[ta * CH]), to_f32(dl_s[tb * CH])),
+                                 f2(bias_c, bias_c));
+          if constexpr (decltype(with_softplus)::value) d2 = softplus2<kBf16Io>(d2);
+          d2 = f2(ta < t_valid ? d2.x : 0.f, tb < t_valid ? d2.y : 0.f);
+          const float2 du = __fmul2_rn(d2, u2);
+          own_dt[k] = d2.x;
+          own_dt[k + 1] = d2.y;
+          own_du[k] = du.x;
+          own_du[k + 1] = du.y;
+          own_u[k] = u2.x;
+          own_u[k + 1] = u2.y;
+        }
+      };
+      if (p.softplus)  // one branch per chunk, not per step pair
+        prologue(std::true_type{});
+      else
+        prologue(std::false_type{});
       // The summed step of every re-anchoring window (kAnchorW steps): each lane sums the
       // window's steps it computed; with G lanes per channel the partial sums are combined by
       // log2 G exchanges, which give all G lanes the same value (the additions see the same
@@ -681,15 +688,21 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
       IO* yw = ywarp0 + size_t(ystores & 1) * (size_t(W) * lay.y_warp / sizeof(IO));
       float yo[OWN];
       reduce_transpose<G, TC>(ys, yo, g);
+      auto epilogue = [&](auto with_gate) {
 #pragma unroll
-      for (int k = 0; k < OWN; k += 2) {
-        const int ta = g + G * k, tb = ta + G;  // this lane's steps
-        float2 y2 = __ffma2_rn(f2(D_c, D_c), f2(uo[k], uo[k + 1]), f2(yo[k], yo[k + 1]));
-        if (p.has_z)
-          y2 = __fmul2_rn(y2, silu2(f2(to_f32(z_s[ta * CH]), to_f32(z_s[tb * CH]))));
-        store_io(yw + ta * CPW + lane / G, y2.x);
-        store_io(yw + tb * CPW + lane / G, y2.y);
-      }
+        for (int k = 0; k < OWN; k += 2) {
+          const int ta = g + G * k, tb = ta + G;  // this lane's steps
+          float2 y2 = __ffma2_rn(f2(D_c, D_c), f2(uo[k], uo[k + 1]), f2(yo[k], yo[k + 1]));
+          if constexpr (decltype(with_gate)::value)
+            y2 = __fmul2_rn(y2, silu2(f2(to_f32(z_s[ta * CH]), to_f32(z_s[tb * CH]))));
+          store_io(yw + ta * CPW + lane / G, y2.x);
+          store_io(yw + tb * CPW + lane / G, y2.y);
+        }
+      };
+      if (p.has_z)  // one branch per chunk
+        epilogue(std::true_type{});
+      else
+        epilogue(std::false_type{});
       fence_smem_to_async();
       release_stage(s, q);  // z was the stage's last use
       if (lane == 0) {
