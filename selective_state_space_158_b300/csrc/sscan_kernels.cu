@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
       constexpr bool kScalarArgs = G == 4;   // dt, dt u kept as scalars (registers)
       constexpr int NP = kShare ? OWN : TC;  // steps this lane computes
       float own_dt[NP], own_du[NP], own_u[NP], uo[OWN];
-      auto prologue = [&](auto with_softplus) {
+      auto prologue = [&](auto with_softplus, auto masked) {
 #pragma unroll
         for (int k = 0; k < NP; k += 2) {
           const int ta = kShare ? g + G * k : k, tb = kShare ? ta + G : k + 1;
@@ -506,7 +506,8 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
           float2 d2 = __fadd2_rn(f2(to_f32(dl_s[ta * CH]), to_f32(dl_s[tb * CH])),
                                  f2(bias_c, bias_c));
           if constexpr (decltype(with_softplus)::value) d2 = softplus2<kBf16Io>(d2);
-          d2 = f2(ta < t_valid ? d2.x : 0.f, tb < t_valid ? d2.y : 0.f);
+          if constexpr (decltype(masked)::value)  // the sequence's last chunk only
+            d2 = f2(ta < t_valid ? d2.x : 0.f, tb < t_valid ? d2.y : 0.f);
           const float2 du = __fmul2_rn(d2, u2);
           own_dt[k] = d2.x;
           own_dt[k + 1] = d2.y;
@@ -516,10 +517,19 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
           own_u[k + 1] = u2.y;
         }
       };
-      if (p.softplus)  // one branch per chunk, not per step pair
-        prologue(std::true_type{});
-      else
-        prologue(std::false_type{});
+      // One branch per chunk on the softplus flag and on whether the chunk runs past the end
+      // of the sequence, instead of tests per step pair.
+      if (t_valid == TC) {
+        if (p.softplus)
+          prologue(std::true_type{}, std::false_type{});
+        else
+          prologue(std::false_type{}, std::false_type{});
+      } else {
+        if (p.softplus)
+          prologue(std::true_type{}, std::true_type{});
+        else
+          prologue(std::false_type{}, std::true_type{});
+      }
       // The summed step of every re-anchoring window (kAnchorW steps): each lane sums the
       // window's steps it computed; with G lanes per channel the partial sums are combined by
       // log2 G exchanges, which give all G lanes the same value (the additions see the same
