@@ -589,7 +589,41 @@ def measure_rates(index: int = 0) -> dict:
             out[name] = {"ex2_per_clk_sm": 1024 * iters * e.value / med,
                          "fp32_per_clk_sm": 1024 * iters * f.value / med,
                          "cycles_median": med, "cycles_spread": [int(cyc.min()), int(cyc.max())]}
+        out["step_loop"] = step_loop_rates(lib, sms)
     return out
+
+
+def step_loop_rates(lib, sms: int, chunks: int = 256) -> dict:
+    """The scan's step loop alone (libsscan_peaks step-loop probe: states in registers, the
+    step's (dt, dt u) and B/C rows from shared memory, no HBM traffic, no prologue or epilogue),
+    in state updates per SM and clock, for 16 and 8 states per lane, with and without the readout,
+    at 8, 16 and 24 resident warps per SM. Per SM: the updates of its CTAs over the span from the
+    first start to the last end on its own clock; the median over SMs."""
+    import ctypes
+
+    import numpy as np
+
+    fn = lib.sscan_peaks_step_loop
+    fn.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    res = {}
+    for k in (16, 8):
+        for readout in (1, 0):
+            for wps in (8, 16, 24):
+                blocks = sms * wps // 4
+                smid = np.zeros(blocks, dtype=np.uint32)
+                clk = np.zeros(2 * blocks, dtype=np.int64)
+                rc = fn(k, readout, blocks, chunks, smid.ctypes.data, clk.ctypes.data)
+                if rc != 0:
+                    raise RuntimeError(f"step-loop probe failed: CUDA error {rc}")
+                per_sm = []
+                for sm in np.unique(smid):
+                    m = smid == sm
+                    span = int(clk[1::2][m].max() - clk[0::2][m].min())
+                    per_sm.append(int(m.sum()) * 128 * k * 16 * chunks / span)
+                name = f"states{k}_{'readout' if readout else 'no_readout'}_warps{wps}"
+                res[name] = float(np.median(per_sm))
+    return res
 
 
 def update_peak(rates: dict, sms: int, mhz: float) -> dict:
@@ -603,6 +637,7 @@ def update_peak(rates: dict, sms: int, mhz: float) -> dict:
             "fp32_per_clk_sm": r_fma, "updates_per_clk_sm": per_clk,
             "binding_pipe": "SFU" if r_ex2 <= r_fma / FP32_OPS_PER_UPDATE else "FP32",
             "mix_updates_per_clk_sm": rates["mix_packed"]["ex2_per_clk_sm"],
+            "step_loop_updates_per_clk_sm": rates["step_loop"]["states16_readout_warps24"],
             "source": f"libsscan_peaks probes on this GPU x {sms} SMs x {mhz:.0f} MHz (max SM "
                       f"clock)"}
 
@@ -625,6 +660,10 @@ def scan_roofline(w, sec_per_launch: float, peak: dict, hbm_gbs: float, peak_src
                 "peak_source": peak["source"]}
     roof["hbm_frac"] = gbs / hbm_gbs
     roof["alu_frac"] = ups / peak["updates_per_s"]
+    # the scan's step loop alone (no HBM, no prologue / epilogue), 24 warps per SM: the practical
+    # ceiling of this instruction mix, for context
+    loop_ups = peak["step_loop_updates_per_clk_sm"] * peak["sms"] * peak["mhz"] * 1e6
+    roof["step_loop_frac"] = ups / loop_ups
     roof["algorithmic_bytes"] = bytes_
     roof["t_hbm_ms"] = t_hbm * 1e3
     roof["t_alu_ms"] = t_alu * 1e3

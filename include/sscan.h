@@ -37,7 +37,7 @@ typedef enum { SSCAN_DISC_ZOH = 0, SSCAN_DISC_EULER = 1 } sscan_disc_t;
 typedef enum {
   SSCAN_OK = 0,
   SSCAN_ERR_INVALID_ARG = 1,   /* null required pointer, negative size, N outside 1..16, ... */
-  SSCAN_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve (no such case today) */
+  SSCAN_ERR_UNSUPPORTED = 2,   /* reserved: no entry point of this version returns it */
   SSCAN_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
   SSCAN_ERR_CARRY_TIMEOUT = 4, /* device side: a bounded wait (pipeline or chunk carry) ran out */
   SSCAN_ERR_SCRATCH_TOO_SMALL = 5 /* sscan_fwd_noalloc: the call needs more scratch than the

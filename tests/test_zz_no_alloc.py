@@ -73,18 +73,20 @@ def test_noalloc_matches_oracle_and_sscan_fwd_twice_in_a_row(key, tune):
     y = torch.empty_like(x["u"])
     h = torch.empty_like(h_ref)
     assert _noalloc(lib, x, y, h) == 0  # warm-up: the first call on a device does its set-up
-    torch.cuda.synchronize()
-    free0, used0 = torch.cuda.mem_get_info()[0], _pool_used_bytes()
     for call in range(2):
         y.fill_(float("nan"))
         h.fill_(float("nan"))
+        # Free device memory and the default pool's use are read right around the call: the
+        # checks in between (torch's own temporaries) may grow torch's cache.
+        torch.cuda.synchronize()
+        free0, used0 = torch.cuda.mem_get_info()[0], _pool_used_bytes()
         assert _noalloc(lib, x, y, h) == 0, f"call {call}"
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0, f"call {call} changed free device memory"
+        assert _pool_used_bytes() == used0, f"call {call} used the default pool"
         assert binding.device_error() == 0
         assert_within(compare(y, h, yr, hr, w.io, y_mag=ym), w.io, f"noalloc call {call} vs oracle")
         assert torch.equal(y, y_ref) and torch.equal(h, h_ref), f"call {call} vs sscan_fwd"
-    torch.cuda.synchronize()
-    assert torch.cuda.mem_get_info()[0] == free0
-    assert _pool_used_bytes() == used0
 
 
 def test_noalloc_plain_load_path(tune):
