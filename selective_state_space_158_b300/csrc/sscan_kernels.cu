@@ -17,6 +17,7 @@
 //   * sscan_simple_kernel: one thread per channel with plain loads; serves any alignment, any
 //     dim and any N <= 16.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -919,11 +920,21 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   // into enough segments for about 256 warps per SM in total, i.e. many short waves of resident
   // CTAs: measured on B300 for the long sequence (batch 1, L 2^20, D 1536, two lanes per
   // channel), 62 segments 12.6 ms, 123 11.6 ms, 246 11.4 ms, 492 11.25 ms, 740 11.2 ms.
+  // But the prefix passes from one segment to the next in about 2.5 us (measured), so the chain
+  // of n_seg segments costs n_seg x 2.5 us however few channels there are: with few channels
+  // (batch 1, D 64, L 2^20: 9472 segments by the rule above, 19.8 ms; 256 segments 1.28 ms)
+  // the count is capped at the larger of sqrt(L / 10) (chain and per-segment time balanced,
+  // measured) and the count whose chain takes a tenth of the two passes' time at about
+  // 4.8e12 updates/s.
   int n_seg = segments;
   if (n_seg <= 0) {
     n_seg = 1;
-    if (units_per_seg < kSplitBelowWarps)
-      n_seg = int((148 * 256 + units_per_seg - 1) / units_per_seg);
+    if (units_per_seg < kSplitBelowWarps) {
+      const double fill = std::ceil(148.0 * 256.0 / double(units_per_seg));
+      const double two_pass_us = 2.0 * double(a.batch) * double(a.L) * double(a.dim) * kNP / 4.8e6;
+      const double by_chain = std::max(std::sqrt(double(a.L) / 10.0), 0.1 * two_pass_us / 2.5);
+      n_seg = int(std::max(1.0, std::min(fill, std::ceil(by_chain))));
+    }
   }
   n_seg = std::max(1, std::min(n_seg, std::max(1, p.n_chunks / 4)));
   p.seg_chunks = (p.n_chunks + n_seg - 1) / n_seg;
