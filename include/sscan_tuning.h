@@ -34,6 +34,9 @@ typedef struct {
   int test_skip_publish; /* fault injection: the time segment with this index never publishes
                             its chunk-carry summary, so that its successors' bounded waits run
                             out and report SSCAN_ERR_CARRY_TIMEOUT (-1: off) */
+  int time_scan;         /* forward: 1 = the time-lane kernel (a warp scans one channel over
+                            time, the lanes' aggregates composed in order), 2 = never, 0 = auto;
+                            calls that write backward checkpoints never use it */
 } sscan_tuning_t;
 
 /* Installs *t (NULL: back to every automatic choice, hook off). Returns SSCAN_ERR_INVALID_ARG

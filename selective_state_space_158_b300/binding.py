@@ -46,7 +46,7 @@ class Tuning(ctypes.Structure):
                 ("threads", ctypes.c_int), ("stages", ctypes.c_int), ("chunk", ctypes.c_int),
                 ("force_plain", ctypes.c_int), ("bwd_segments", ctypes.c_int),
                 ("conv_plain", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("test_skip_publish", ctypes.c_int)]
+                ("test_skip_publish", ctypes.c_int), ("time_scan", ctypes.c_int)]
 
 
 _TUNING_P = ctypes.POINTER(Tuning)

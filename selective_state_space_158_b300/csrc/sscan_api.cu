@@ -107,7 +107,7 @@ sscan_status_t sscan_set_tuning(const sscan_tuning_t* t) {
         t->threads > 256 || t->threads % 32 != 0 || t->stages < 0 || t->stages > 8 ||
         t->stages == 1 || (t->chunk != 0 && t->chunk != 16 && t->chunk != 32) ||
         t->bwd_segments < 0 || t->test_skip_publish < -1 || t->ctas_per_sm < 0 ||
-        t->ctas_per_sm > 32)
+        t->ctas_per_sm > 32 || t->time_scan < 0 || t->time_scan > 2)
       return SSCAN_ERR_INVALID_ARG;
     n.states_per_lane = k;
     n.segments = t->segments;
@@ -119,6 +119,7 @@ sscan_status_t sscan_set_tuning(const sscan_tuning_t* t) {
     n.conv_plain = t->conv_plain != 0;
     n.ctas_per_sm = t->ctas_per_sm;
     n.skip_publish = t->test_skip_publish;
+    n.time_scan = t->time_scan;
   }
   std::lock_guard<std::mutex> lk(g_tune_mu);
   g_tune = n;
@@ -145,6 +146,7 @@ sscan_status_t sscan_get_tuning(sscan_tuning_t* t) {
   t->conv_plain = c.conv_plain;
   t->ctas_per_sm = c.ctas_per_sm;
   t->test_skip_publish = c.skip_publish;
+  t->time_scan = c.time_scan;
   return SSCAN_OK;
 }
 

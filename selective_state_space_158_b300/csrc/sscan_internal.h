@@ -51,6 +51,7 @@ struct Tuning {
   int conv_plain = 0;         // Conv1d: register-window kernel only
   int ctas_per_sm = 0;        // forward: cap on resident CTAs per SM (0: no cap)
   int skip_publish = -1;      // test hook: this segment never publishes its aggregate
+  int time_scan = 0;          // forward: 1 time-lane kernel, 2 never, 0 automatic
 };
 
 // The setting sscan_set_tuning installed (a copy, taken under the setting's lock).

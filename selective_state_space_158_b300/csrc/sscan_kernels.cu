@@ -743,6 +743,421 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
     for (int s = 0; s < S && s < n_loads; ++s) mbar_wait_bounded(&full[s], 0, 100000);
 }
 
+// ================================================================================================
+// Time lanes: the scan over time inside a warp. One warp scans one channel; its 32 lanes are 32
+// consecutive stretches of kTsT steps of a kTsChunk-step chunk, each lane holding all 16 states.
+// Per chunk:
+//   1. every lane runs its kTsT steps from a zero state: its aggregate (P, H), H the end state
+//      and P = 2^(A log2e S) the decay over its steps (S their summed step; the product of the
+//      factors for the first order);
+//   2. the 32 aggregates are composed in order with (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2)
+//      ("架构变体：Mamba/SSM", "硬件感知算法": the update is associative), starting from the
+//      state the warp carries into the chunk: lane n < 16 walks the 32 aggregates of state n
+//      through shared memory and leaves every lane's start state there, and the chunk's end
+//      state is the carry into the next chunk;
+//   3. every lane runs its kTsT steps again from its true start state, with the readout, skip,
+//      gate and stores.
+// A CTA is kTsW warps (kTsW consecutive channels: the TMA boxes are kTsChunk steps x kTsW
+// channels). Each lane reads a different step, so the staged tiles are first regrouped by the
+// whole CTA into layouts where a lane's steps are contiguous (u, delta, z and y channel-major;
+// B and C as [quad of states][lane][step + 1 pad] float4) and the warp's accesses hit distinct
+// shared-memory banks. Long sequences with few channels are split into time segments joined by
+// the same chained carry as the lane kernel: a segment with a successor first runs steps 1-2 over
+// all its chunks (its aggregate), then waits for its predecessor's prefix and publishes its own.
+// fp32 io composes the lanes with the accurate exponential, so the SFU's rounding compounds over
+// at most kTsT steps.
+// ================================================================================================
+constexpr int kTsT = 8;               // steps per lane and chunk
+constexpr int kTsChunk = 32 * kTsT;   // steps per chunk
+constexpr int kTsW = 8;               // warps (channels) per CTA
+constexpr int kTsPad = kTsT + 1;      // float4 slots per lane and quad of states (one pad)
+
+struct TsSmem {
+  size_t tile_io, bc, stage, off_t, t_io, off_bt, bt, off_scan, scan_warp, off_y, y_tile, off_bar,
+      total;
+  __host__ __device__ TsSmem(int es, int stages) {
+    tile_io = align128(size_t(kTsChunk) * kTsW * es);      // TMA tile [kTsChunk][kTsW] io
+    bc = align128(size_t(kTsChunk) * kNP * sizeof(float));  // TMA tile [kTsChunk][16] fp32
+    stage = 3 * tile_io + 2 * bc;                           // u, delta, z; B, C
+    off_t = size_t(stages) * stage;                         // u, delta, z as [kTsW][kTsChunk]
+    t_io = align128(size_t(kTsW) * kTsChunk * es);          // (y reuses u's: see the kernel)
+    off_bt = off_t + 3 * t_io;                              // B, C as [4][32][kTsPad] float4
+    bt = align128(size_t(4) * 32 * kTsPad * 4 * sizeof(float));
+    off_scan = off_bt + 2 * bt;
+    scan_warp = align128((2 * 32 * kNP + 32) * sizeof(float));  // P, H [32][16]; S [32]
+    off_y = off_scan + size_t(kTsW) * scan_warp;                // two y tiles [kTsChunk][kTsW]
+    y_tile = align128(size_t(kTsChunk) * kTsW * es);
+    off_bar = off_y + 2 * y_tile;
+    total = off_bar + 8 * 8;  // full[8]
+  }
+};
+
+// Eight io values at a 16-byte aligned address (fp32: 32 bytes) to and from floats.
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // element 2i in the low half of word i
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);  // .x the low half
+    w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename IO, bool EULER>
+__global__ void __launch_bounds__(kTsW * 32, 1)
+    sscan_tscan_kernel(const __grid_constant__ CUtensorMap tm_u,
+                       const __grid_constant__ CUtensorMap tm_dl,
+                       const __grid_constant__ CUtensorMap tm_z,
+                       const __grid_constant__ CUtensorMap tm_B,
+                       const __grid_constant__ CUtensorMap tm_C,
+                       const __grid_constant__ CUtensorMap tm_y, const LaneParams p) {
+  constexpr float kScaleA = EULER ? 1.f : kLog2e;
+  constexpr float kArg = EULER ? 1.f : 0.f;
+  constexpr bool kAccurate = std::is_same<IO, float>::value && !EULER;
+  constexpr bool kBf16Io = !std::is_same<IO, float>::value;
+  constexpr int KP = kNP / 2;
+  auto decay = [](float2 arg) -> float2 {
+    if constexpr (EULER)
+      return arg;
+    else
+      return f2(ex2(arg.x), ex2(arg.y));
+  };
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = p.N, S = p.stages;
+  const TsSmem lay(int(sizeof(IO)), S);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.off_bar);
+  __shared__ unsigned s_ticket;
+
+  int cgi, b, seg;
+  if (p.n_seg == 1) {
+    cgi = blockIdx.x;
+    b = blockIdx.y;
+    seg = 0;
+  } else {
+    if (tid == 0) s_ticket = atomicAdd(p.ticket, 1u);
+    __syncthreads();
+    const unsigned t = s_ticket;  // segment-major: every earlier segment got an earlier ticket
+    const unsigned per_seg = unsigned(p.batch) * unsigned(p.n_cg);
+    seg = int(t / per_seg);
+    b = int((t % per_seg) / unsigned(p.n_cg));
+    cgi = int(t % unsigned(p.n_cg));
+  }
+  const int ch0 = cgi * kTsW;
+  const int c_begin = seg * p.seg_chunks;
+  const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
+  const int nch = c_end - c_begin;
+  const bool agg_pass = p.n_seg > 1 && seg + 1 < p.n_seg;
+  const int n_loads = (agg_pass ? 2 : 1) * nch;
+
+  auto stage_ptr = [&](int s, int which) -> unsigned char* {  // 0 u, 1 delta, 2 z, 3 B, 4 C
+    unsigned char* base = smem + size_t(s) * lay.stage;
+    return which < 3 ? base + size_t(which) * lay.tile_io
+                     : base + 3 * lay.tile_io + size_t(which - 3) * lay.bc;
+  };
+  IO* tU = reinterpret_cast<IO*>(smem + lay.off_t);  // [kTsW][kTsChunk]; also y before its store
+  IO* tD = reinterpret_cast<IO*>(smem + lay.off_t + lay.t_io);
+  IO* tZ = reinterpret_cast<IO*>(smem + lay.off_t + 2 * lay.t_io);
+  float4* tB = reinterpret_cast<float4*>(smem + lay.off_bt);  // [4][32][kTsPad]
+  float4* tC = reinterpret_cast<float4*>(smem + lay.off_bt + lay.bt);
+  const uint32_t tile_bytes = uint32_t(kTsChunk) * kTsW * sizeof(IO);
+  const uint32_t bc_bytes = uint32_t(kTsChunk) * kNP * sizeof(float);
+  // Load q brings chunk c_begin + q % nch into stage s (the aggregate pass needs no gate z).
+  auto issue_load = [&](int q, int s) {
+    const bool with_z = p.has_z && !(agg_pass && q < nch);
+    const int t0 = (c_begin + (q < nch ? q : q - nch)) * kTsChunk;
+    mbar_arrive_expect_tx(&full[s], (with_z ? 3u : 2u) * tile_bytes + 2u * bc_bytes);
+    tma_load_3d(stage_ptr(s, 0), &tm_u, ch0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 1), &tm_dl, ch0, t0, b, &full[s]);
+    if (with_z) tma_load_3d(stage_ptr(s, 2), &tm_z, ch0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 3), &tm_B, 0, t0, b, &full[s]);
+    tma_load_3d(stage_ptr(s, 4), &tm_C, 0, t0, b, &full[s]);
+  };
+  // Regroups an io tile [kTsChunk][kTsW] into [kTsW][kTsChunk]: thread r takes row r.
+  auto regroup_io = [&](const IO* tile, IO* dst) {
+    float v[8];
+    load8(tile + tid * kTsW, v);
+#pragma unroll
+    for (int w = 0; w < kTsW; ++w) store_io(dst + w * kTsChunk + tid, v[w]);
+  };
+  // Regroups a B or C tile [kTsChunk][16] into [quad][lane][step]: float4 (row r, quad q) goes
+  // to lane r / kTsT, slot r % kTsT.
+  auto regroup_bc = [&](const float* tile, float4* dst) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + i * (kTsW * 32), r = idx >> 2, qd = idx & 3;
+      dst[(qd * 32 + r / kTsT) * kTsPad + r % kTsT] = reinterpret_cast<const float4*>(tile)[idx];
+    }
+  };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int q = 0; q < S && q < n_loads; ++q) issue_load(q, q);
+
+  const int cg = ch0 + warp;  // this warp's channel
+  const bool live = cg < p.dim;
+  float2 A2[KP];
+#pragma unroll
+  for (int r = 0; r < KP; ++r) {
+    const int n = 2 * r;
+    A2[r] = f2((live && n < N) ? p.A[size_t(cg) * N + n] * kScaleA : 0.f,
+               (live && n + 1 < N) ? p.A[size_t(cg) * N + n + 1] * kScaleA : 0.f);
+  }
+  const float bias_c = (p.bias && live) ? p.bias[cg] : 0.f;
+  const float D_c = (p.D && live) ? p.D[cg] : 0.f;
+  // Lane n < 16 carries state n across chunks (and segments); a_n is its A log2e (or A).
+  const bool scanner = lane < kNP;
+  const float a_n = (live && lane < N) ? p.A[size_t(cg) * N + lane] * kScaleA : 0.f;
+  const float hz = (p.h0 && live && lane < N) ? p.h0[(size_t(b) * p.dim + cg) * N + lane] : 0.f;
+  float carry = seg == 0 ? hz : 0.f;
+  float* scanP = reinterpret_cast<float*>(smem + lay.off_scan + size_t(warp) * lay.scan_warp);
+  float* scanH = scanP + 32 * kNP;
+  float* scanS = scanH + 32 * kNP;
+  IO* ytile0 = reinterpret_cast<IO*>(smem + lay.off_y);
+  const float4* bq_l = tB + lane * kTsPad;  // this lane's B, C slots: quad qd at + qd 32 kTsPad
+  const float4* cq_l = tC + lane * kTsPad;
+
+  bool timed_out = false;
+  float sd = 0.f, sd_c = 0.f;  // Kahan sum of the segment's steps (aggregate pass)
+  float pprod = 1.f;           // first order: product of the segment's factors of state n
+  int q = 0, s = 0;
+  uint32_t phase = 0;
+  int ystores = 0;
+  const size_t unit = ((size_t(seg) * p.batch + b) * p.n_cg + cgi) * kTsW + warp;
+  const size_t units_per_seg = size_t(p.batch) * p.n_cg * kTsW;
+  for (int pass = agg_pass ? 0 : 1; pass < 2 && !timed_out; ++pass) {
+    const bool readout = pass == 1;
+    if (readout && p.n_seg > 1) {
+      // Chunk carry between segments, as in the lane kernel: segment s > 0 waits for segment
+      // s - 1's inclusive prefix and, with a successor, publishes its own,
+      // 2^(A log2e SD_s) h_in + H_s (the product of its factors for the first order).
+      float start = hz;
+      if (seg > 0) {
+        const size_t up = unit - units_per_seg;
+        unsigned f = 0;
+        if (lane == 0) {
+          for (uint32_t it = 0; it < kLookbackTries; ++it) {
+            f = ld_acquire(p.flags + up);
+            if (f != 0) break;
+            __nanosleep(512);
+          }
+          if (f == 0) atomicOr(p.status, kErrCarry);
+        }
+        f = __shfl_sync(0xffffffffu, f, 0);
+        start = (f != 0 && scanner) ? __ldcg(p.agg + up * kNP + lane) : 0.f;
+      }
+      if (agg_pass && seg != p.skip_publish) {
+        float incl = carry;  // segment 0: the end state from h0 already
+        if (seg > 0) {
+          float P;
+          if constexpr (EULER)
+            P = pprod;
+          else if constexpr (kAccurate)
+            P = exp2_acc(a_n * sd);
+          else
+            P = ex2(a_n * sd);
+          incl = fmaf(P, start, carry);
+        }
+        if (scanner) p.agg[unit * kNP + lane] = incl;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release(p.flags + unit, kFlagAgg);
+      }
+      carry = start;
+    }
+    for (int ci = 0; ci < nch; ++ci, ++q, s = (s + 1 == S) ? 0 : s + 1, phase ^= (s == 0)) {
+      const int t0 = (c_begin + ci) * kTsChunk;
+      const bool landed = mbar_wait_bounded(&full[s], phase, kWaitNs);
+      // CTA-uniform exit; it also orders every warp's reads of the regrouped tiles of the
+      // previous chunk before they are overwritten.
+      if (__syncthreads_or(!landed)) {
+        timed_out = true;
+        break;
+      }
+      regroup_io(reinterpret_cast<const IO*>(stage_ptr(s, 0)), tU);
+      regroup_io(reinterpret_cast<const IO*>(stage_ptr(s, 1)), tD);
+      if (readout && p.has_z) regroup_io(reinterpret_cast<const IO*>(stage_ptr(s, 2)), tZ);
+      regroup_bc(reinterpret_cast<const float*>(stage_ptr(s, 3)), tB);
+      if (readout) regroup_bc(reinterpret_cast<const float*>(stage_ptr(s, 4)), tC);
+      __syncthreads();  // the stage is consumed; the regrouped tiles are complete
+      if (tid == 0 && q + S < n_loads) {
+        fence_smem_to_async();
+        issue_load(q + S, s);
+      }
+      const int row0 = lane * kTsT;  // this lane's first step in the chunk
+      // The lane's steps: dt = softplus(delta + bias) (0 past the sequence end), dt u, u, and
+      // SiLU(z) (1 without gate) for the readout.
+      float uo[kTsT], dt[kTsT], du[kTsT], sil[kTsT];
+      load8(tU + warp * kTsChunk + row0, uo);
+      load8(tD + warp * kTsChunk + row0, dt);
+      const int tv = p.L - (t0 + row0);  // this lane's steps inside the sequence
+#pragma unroll
+      for (int k = 0; k < kTsT; k += 2) {
+        float2 d2 = __fadd2_rn(f2(dt[k], dt[k + 1]), f2(bias_c, bias_c));
+        if (p.softplus) d2 = softplus2<kBf16Io>(d2);
+        d2 = f2(k < tv ? d2.x : 0.f, k + 1 < tv ? d2.y : 0.f);
+        const float2 d2u = __fmul2_rn(d2, f2(uo[k], uo[k + 1]));
+        dt[k] = d2.x;
+        dt[k + 1] = d2.y;
+        du[k] = d2u.x;
+        du[k + 1] = d2u.y;
+        sil[k] = 1.f;
+        sil[k + 1] = 1.f;
+      }
+      if (readout && p.has_z) {
+        float zv[kTsT];
+        load8(tZ + warp * kTsChunk + row0, zv);
+#pragma unroll
+        for (int k = 0; k < kTsT; k += 2) {
+          const float2 sz = silu2(f2(zv[k], zv[k + 1]));
+          sil[k] = sz.x;
+          sil[k + 1] = sz.y;
+        }
+      }
+      // 1. The lane's steps from a zero state: its aggregate.
+      float2 h[KP], Pp[EULER ? KP : 1];
+#pragma unroll
+      for (int r = 0; r < KP; ++r) {
+        h[r] = f2(0.f, 0.f);
+        if constexpr (EULER) Pp[r] = f2(1.f, 1.f);
+      }
+      float ssum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kTsT; ++k) {
+        ssum += dt[k];
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          const float4 bq = bq_l[qd * 32 * kTsPad + k];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int r = 2 * qd + j;
+            const float2 dA = decay(__ffma2_rn(f2(dt[k], dt[k]), A2[r], f2(kArg, kArg)));
+            const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
+            h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(f2(du[k], du[k]), bb));
+            if constexpr (EULER) Pp[r] = __fmul2_rn(Pp[r], dA);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < KP; r += 2) {
+        float2 P0, P1;
+        if constexpr (EULER) {
+          P0 = Pp[r];
+          P1 = Pp[r + 1];
+        } else if constexpr (kAccurate) {
+          P0 = exp2_acc2(__fmul2_rn(A2[r], f2(ssum, ssum)));
+          P1 = exp2_acc2(__fmul2_rn(A2[r + 1], f2(ssum, ssum)));
+        } else {
+          P0 = f2(ex2(A2[r].x * ssum), ex2(A2[r].y * ssum));
+          P1 = f2(ex2(A2[r + 1].x * ssum), ex2(A2[r + 1].y * ssum));
+        }
+        *reinterpret_cast<float4*>(scanP + lane * kNP + 2 * r) = make_float4(P0.x, P0.y, P1.x, P1.y);
+        *reinterpret_cast<float4*>(scanH + lane * kNP + 2 * r) =
+            make_float4(h[r].x, h[r].y, h[r + 1].x, h[r + 1].y);
+      }
+      scanS[lane] = ssum;
+      __syncwarp();
+      // 2. Compose the 32 aggregates of state n in order (lane n < 16), from the carry; every
+      //    lane's start state replaces its P.
+      if (scanner) {
+        float x = carry;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+          const float pj = scanP[j * kNP + lane], hj = scanH[j * kNP + lane];
+          scanP[j * kNP + lane] = x;
+          x = fmaf(pj, x, hj);
+          if (!readout) {
+            if constexpr (EULER) pprod *= pj;
+            const float yk = scanS[j] - sd_c;  // Kahan step of the segment's summed step
+            const float tk = sd + yk;
+            sd_c = (tk - sd) - yk;
+            sd = tk;
+          }
+        }
+        carry = x;
+      }
+      __syncwarp();
+      if (readout) {
+        // 3. The lane's steps again from its start state, with the readout; y into the lane's
+        //    slots of the regrouped u (read above), then regrouped into the TMA tile.
+#pragma unroll
+        for (int r = 0; r < KP; r += 2) {
+          const float4 hv = *reinterpret_cast<const float4*>(scanP + lane * kNP + 2 * r);
+          h[r] = f2(hv.x, hv.y);
+          h[r + 1] = f2(hv.z, hv.w);
+        }
+        float yv[kTsT];
+#pragma unroll
+        for (int k = 0; k < kTsT; ++k) {
+          float2 acc = f2(0.f, 0.f);
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            const float4 bq = bq_l[qd * 32 * kTsPad + k], cq = cq_l[qd * 32 * kTsPad + k];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int r = 2 * qd + j;
+              const float2 dA = decay(__ffma2_rn(f2(dt[k], dt[k]), A2[r], f2(kArg, kArg)));
+              const float2 bb = j ? f2(bq.z, bq.w) : f2(bq.x, bq.y);
+              const float2 cc = j ? f2(cq.z, cq.w) : f2(cq.x, cq.y);
+              h[r] = __ffma2_rn(dA, h[r], __fmul2_rn(f2(du[k], du[k]), bb));
+              acc = __ffma2_rn(cc, h[r], acc);
+            }
+          }
+          yv[k] = fmaf(D_c, uo[k], acc.x + acc.y) * sil[k];
+        }
+        store8(tU + warp * kTsChunk + row0, yv);
+        __syncthreads();  // every warp's y is in tU
+        IO* yt = ytile0 + size_t(ystores & 1) * (lay.y_tile / sizeof(IO));
+        {
+          float v[8];
+#pragma unroll
+          for (int w = 0; w < kTsW; ++w) v[w] = to_f32(tU[w * kTsChunk + tid]);
+          store8(yt + tid * kTsW, v);
+        }
+        fence_smem_to_async();  // this thread's y row before the tile's TMA store
+        __syncthreads();
+        if (tid == 0) {
+          tma_store_3d(&tm_y, yt, ch0, t0, b);
+          tma_store_commit();
+          tma_store_wait_read<1>();  // the other tile, written next, has been read
+        }
+        ++ystores;
+      }
+    }
+  }
+
+  if (timed_out) {
+    if (tid == 0) atomicOr(p.status, kErrTimeout);
+  } else if (p.h_last && live && scanner && lane < N && seg == p.n_seg - 1) {
+    p.h_last[(size_t(b) * p.dim + cg) * N + lane] = carry;
+  }
+  if (tid == 0) tma_store_wait_all();
+  const int any_timeout = __syncthreads_or(timed_out);
+  if (tid == 0 && any_timeout)
+    for (int s2 = 0; s2 < S && s2 < n_loads; ++s2) mbar_wait_bounded(&full[s2], 0, 100000);
+}
+
 // B and C widened once per call to fp32 rows of 16 states (zero-padded past N), the layout the
 // scan kernel stages with TMA and reads as 16-byte vectors. One thread per (batch, step) row.
 template <typename IO>
@@ -1014,6 +1429,56 @@ cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, const Tuning& tu
                      : launch_lane_typed<IO, 4, 16, EULER>(a, threads, tune);
 }
 
+// The time-lane kernel: CTAs of kTsW channels; for few channels the sequence is split into
+// about two CTAs per SM in total, capped by the chain of segment prefixes (sqrt(L / 10), as for
+// the lane kernel).
+template <typename IO, bool EULER>
+cudaError_t launch_tscan_typed(const FwdArgs& a, const Tuning& tune) {
+  const int es = int(sizeof(IO));
+  int stages = (tune.stages >= 2 && tune.stages <= 8) ? tune.stages : 3;
+  while (stages > 2 && TsSmem(es, stages).total + 128 > size_t(227) * 1024) --stages;
+  const TsSmem lay(es, stages);
+  const size_t smem_bytes = lay.total + 128;
+  if (smem_bytes > size_t(227) * 1024) return cudaErrorInvalidValue;
+  const int64_t n_cg = (a.dim + kTsW - 1) / kTsW;
+  const int64_t ctas_per_seg = a.batch * n_cg;
+  int segments = tune.segments;
+  if (segments <= 0) {
+    segments = 1;
+    if (ctas_per_seg < 148) {
+      const double fill = std::ceil(2.0 * 148.0 / double(ctas_per_seg));
+      segments = int(std::max(1.0, std::min(fill, std::ceil(std::sqrt(double(a.L) / 10.0)))));
+    }
+  }
+  LaneParams p = base_params(a, kTsW, stages, segments, 0, tune.skip_publish, kTsChunk);
+  Workspace w;
+  cudaError_t e = prepare_workspace(
+      a, p.n_seg > 1 ? size_t(p.n_seg) * size_t(ctas_per_seg) * kTsW : 0, 1, &w);
+  if (e != cudaSuccess) return e;
+  p.ticket = w.ticket;
+  p.flags = w.flags;
+  p.agg = w.agg;
+  CUtensorMap mu, md, mz, mB, mC, my;
+  const uint64_t dim = a.dim, L = a.L, bt = a.batch;
+  bool ok = make_map(&mu, a.u, a.io, dim, L, bt, kTsW, kTsChunk) &&
+            make_map(&md, a.delta, a.io, dim, L, bt, kTsW, kTsChunk) &&
+            make_map(&mz, a.z ? a.z : a.u, a.io, dim, L, bt, kTsW, kTsChunk) &&
+            make_map(&mB, w.B16, Io::F32, kNP, L, bt, kNP, kTsChunk) &&
+            make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, kTsChunk) &&
+            make_map(&my, a.y, a.io, dim, L, bt, kTsW, kTsChunk);
+  if (!ok) return w.release(cudaErrorInvalidValue);
+  auto kern = sscan_tscan_kernel<IO, EULER>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
+  if (e != cudaSuccess) return w.release(e);
+  if (p.n_seg > 1)
+    kern<<<unsigned(p.n_seg * ctas_per_seg), kTsW * 32, smem_bytes, a.stream>>>(mu, md, mz, mB,
+                                                                                  mC, my, p);
+  else
+    kern<<<dim3(unsigned(n_cg), unsigned(bt), 1), kTsW * 32, smem_bytes, a.stream>>>(
+        mu, md, mz, mB, mC, my, p);
+  return w.release(cudaGetLastError());
+}
+
 }  // namespace
 
 cudaError_t launch_lane(const FwdArgs& a, const Tuning& tune) {
@@ -1050,7 +1515,23 @@ bool tma_path_ok(const FwdArgs& a) {
   return get_encode() != nullptr;
 }
 
-cudaError_t launch_tma(const FwdArgs& a, const Tuning& tune) { return launch_lane(a, tune); }
+static cudaError_t launch_tscan(const FwdArgs& a, const Tuning& tune) {
+  if (a.io == Io::F32) return a.euler ? launch_tscan_typed<float, true>(a, tune)
+                                      : launch_tscan_typed<float, false>(a, tune);
+  using bf = __nv_bfloat16;
+  return a.euler ? launch_tscan_typed<bf, true>(a, tune) : launch_tscan_typed<bf, false>(a, tune);
+}
+
+// The time-lane kernel when asked for (it writes no backward checkpoints).
+static bool use_tscan(const FwdArgs& a, const Tuning& tune) {
+  if (a.h_ckpt || tune.time_scan == 2) return false;
+  return tune.time_scan == 1;
+}
+
+cudaError_t launch_tma(const FwdArgs& a, const Tuning& tune) {
+  if (use_tscan(a, tune)) return launch_tscan(a, tune);
+  return launch_lane(a, tune);
+}
 
 cudaError_t launch_forward(const FwdArgs& a) {
   const Tuning tune = current_tuning();
