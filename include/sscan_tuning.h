@@ -35,8 +35,10 @@ typedef struct {
                             its chunk-carry summary, so that its successors' bounded waits run
                             out and report SSCAN_ERR_CARRY_TIMEOUT (-1: off) */
   int time_scan;         /* forward: 1 = the time-lane kernel (a warp scans one channel over
-                            time, the lanes' aggregates composed in order), 2 = never, 0 = auto;
-                            calls that write backward checkpoints never use it */
+                            time, the lanes' aggregates composed in order), 2 = never, 0 = auto
+                            (at most 32 channels, or at most 128 channels and 2^24 channel-steps,
+                            unless states_per_lane, threads or chunk is set); calls that write
+                            backward checkpoints never use it */
 } sscan_tuning_t;
 
 /* Installs *t (NULL: back to every automatic choice, hook off). Returns SSCAN_ERR_INVALID_ARG

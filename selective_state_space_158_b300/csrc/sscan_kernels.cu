@@ -784,8 +784,8 @@ struct TsSmem {
     off_bt = off_t + 3 * t_io;                              // B, C as [4][32][kTsPad] float4
     bt = align128(size_t(4) * 32 * kTsPad * 4 * sizeof(float));
     off_scan = off_bt + 2 * bt;
-    scan_warp = align128((2 * 32 * kNP + 32) * sizeof(float));  // P, H [32][16]; S [32]
-    off_y = off_scan + size_t(kTsW) * scan_warp;                // two y tiles [kTsChunk][kTsW]
+    scan_warp = align128(2 * 32 * kNP * sizeof(float));  // P, H [32][16]
+    off_y = off_scan + size_t(kTsW) * scan_warp;         // two y tiles [kTsChunk][kTsW]
     y_tile = align128(size_t(kTsChunk) * kTsW * es);
     off_bar = off_y + 2 * y_tile;
     total = off_bar + 8 * 8;  // full[8]
@@ -933,7 +933,6 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
   float carry = seg == 0 ? hz : 0.f;
   float* scanP = reinterpret_cast<float*>(smem + lay.off_scan + size_t(warp) * lay.scan_warp);
   float* scanH = scanP + 32 * kNP;
-  float* scanS = scanH + 32 * kNP;
   IO* ytile0 = reinterpret_cast<IO*>(smem + lay.off_y);
   const float4* bq_l = tB + lane * kTsPad;  // this lane's B, C slots: quad qd at + qd 32 kTsPad
   const float4* cq_l = tC + lane * kTsPad;
@@ -1076,7 +1075,15 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
         *reinterpret_cast<float4*>(scanH + lane * kNP + 2 * r) =
             make_float4(h[r].x, h[r].y, h[r + 1].x, h[r + 1].y);
       }
-      scanS[lane] = ssum;
+      if (!readout) {  // the chunk's summed step (a fixed tree), into the segment's Kahan sum
+        float csum = ssum;
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, m);
+        const float yk = csum - sd_c;
+        const float tk = sd + yk;
+        sd_c = (tk - sd) - yk;
+        sd = tk;
+      }
       __syncwarp();
       // 2. Compose the 32 aggregates of state n in order (lane n < 16), from the carry; every
       //    lane's start state replaces its P.
@@ -1087,12 +1094,8 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
           const float pj = scanP[j * kNP + lane], hj = scanH[j * kNP + lane];
           scanP[j * kNP + lane] = x;
           x = fmaf(pj, x, hj);
-          if (!readout) {
-            if constexpr (EULER) pprod *= pj;
-            const float yk = scanS[j] - sd_c;  // Kahan step of the segment's summed step
-            const float tk = sd + yk;
-            sd_c = (tk - sd) - yk;
-            sd = tk;
+          if constexpr (EULER) {
+            if (!readout) pprod *= pj;
           }
         }
         carry = x;
@@ -1522,10 +1525,19 @@ static cudaError_t launch_tscan(const FwdArgs& a, const Tuning& tune) {
   return a.euler ? launch_tscan_typed<bf, true>(a, tune) : launch_tscan_typed<bf, false>(a, tune);
 }
 
-// The time-lane kernel when asked for (it writes no backward checkpoints).
+// The time-lane kernel: when asked for, or automatically for few channels, where the lane
+// kernel's many short time segments are bound by the chain of segment prefixes. Measured on
+// B300 (bf16, batch 1; lane kernel -> time lanes): D 8, L 2^20 1.42 -> 0.72 ms; D 32, L 2^20
+// 1.44 -> 0.89 ms; D 64, L 2^18 0.57 -> 0.44 ms; D 64, L 2^20 1.46 -> 1.59 ms; D 128, L 2^16
+// 0.29 -> 0.22 ms; D 128, L 2^18 0.74 -> 0.97 ms: time lanes for at most 32 channels, or at
+// most 128 channels and 2^24 channel-steps. It writes no backward checkpoints, and an explicit
+// lane layout (states per lane, threads, chunk) keeps the lane kernel.
 static bool use_tscan(const FwdArgs& a, const Tuning& tune) {
   if (a.h_ckpt || tune.time_scan == 2) return false;
-  return tune.time_scan == 1;
+  if (tune.time_scan == 1) return true;
+  if (tune.states_per_lane || tune.threads || tune.chunk) return false;
+  const int64_t chans = a.batch * a.dim;
+  return chans <= 128 && (chans <= 32 || chans * a.L <= (int64_t(1) << 24));
 }
 
 cudaError_t launch_tma(const FwdArgs& a, const Tuning& tune) {

@@ -60,8 +60,10 @@ def test_chunk_carry_segments(segments, K, io, tune):
     check_full(w, what=f"segments={segments} K={K} {io}")
 
 
-def test_chunk_carry_long_sequence_small_width():
-    """Many segments over a long sequence with few channels (the long workload's regime)."""
+def test_chunk_carry_long_sequence_small_width(tune):
+    """Many segments over a long sequence with few channels (the long workload's regime), in
+    the lane kernel (the time-lane kernel would be chosen for this shape)."""
+    tune(time_scan=2)
     w = WORKLOADS["long"].replace(L=1 << 14, dim=64)
     check_full(w, what="long L, narrow")
 
@@ -70,13 +72,13 @@ def test_chunk_carry_timeout_reports_status_and_context_survives(tune):
     """A segment that never publishes makes its successors' bounded look-back waits run out:
     the call finishes, the device status word says SSCAN_ERR_CARRY_TIMEOUT, and the next call
     on the same context is correct again."""
-    tune(segments=3, test_skip_publish=0)
+    tune(segments=3, test_skip_publish=0, time_scan=2)  # the lane kernel's carry
     w = WORKLOADS["fp32"].replace(batch=1, L=200, dim=64)
     x = make_inputs(w, device=DEV)
     binding.fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"])
     assert binding.device_error() == 4
     assert binding.device_error() == 0  # reading clears it
-    tune(segments=3)
+    tune(segments=3, time_scan=2)
     check_full(w, x=x, what="after timeout")
 
 
