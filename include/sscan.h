@@ -181,7 +181,10 @@ sscan_status_t sscan_conv1d_silu(const void* x, const float* w, const float* bia
  * memory gives asynchronous, overlapped copies). The batch is cut into up to 8 slices of whole
  * batch rows that rotate over three streams the library owns (ordered after the work already
  * on `stream`; `stream` waits for all of them), so one slice's copy in, another's scan and a
- * third's copy out overlap; each slice is an independent sscan_fwd over its rows. Device staging
+ * third's copy out overlap; each slice is an independent sscan_fwd over its rows. With fewer
+ * than 8 batch rows and at least 32768 steps the sequence is cut into up to 16 time slices
+ * instead (at least 16384 steps each), copied with strided 2-D copies, and each slice's scan
+ * continues from the previous one's end state (sscan_fwd_ex, in place). Device staging
  * buffers and those streams are owned by the library per device, grown or created on demand and
  * kept until sscan_release(). Calls on one device are serialised inside the library. Returns when
  * y and h_last hold the result, or with the first error (after every copy it queued has ended).

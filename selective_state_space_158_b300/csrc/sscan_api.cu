@@ -2,6 +2,7 @@
 // host-buffer entry point. The operation itself is defined in include/sscan.h.
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/sscan.h"
@@ -13,6 +14,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kHostStreams = 3;      // host path: streams the batch slices rotate over
 constexpr int64_t kHostSlices = 8;   // host path: at most this many batch slices per call
+constexpr int64_t kHostTimeSlices = 16;     // host path, few batch rows: time slices per call
+constexpr int64_t kHostMinSliceSteps = 16384;  // host path: shortest time slice
 
 struct DeviceState {
   unsigned int* status = nullptr;  // device status word
@@ -433,7 +436,10 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
   float* dA = reinterpret_cast<float*>(take(s_A));
   float* dD = D ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
   float* dbias = delta_bias ? reinterpret_cast<float*>(take(s_dim)) : nullptr;
-  float* dh = h_last ? reinterpret_cast<float*>(take(s_h)) : nullptr;
+  // Few batch rows and a long sequence: the sequence is cut into time slices instead, each
+  // continuing from the previous one's end state (dh, always allocated then).
+  const bool by_time = batch < kHostSlices && L >= 2 * kHostMinSliceSteps;
+  float* dh = (h_last || by_time) ? reinterpret_cast<float*>(take(s_h)) : nullptr;
   auto copy = [](void* dst, const void* src, size_t n, cudaMemcpyKind kind, cudaStream_t s) {
     return n == 0 || cudaMemcpyAsync(dst, src, n, kind, s) == cudaSuccess;
   };
@@ -451,6 +457,64 @@ sscan_status_t sscan_fwd_host(const void* u, const void* delta, const float* A, 
   ok = ok && cudaEventRecord(ev_start, stream) == cudaSuccess;
   for (int k = 0; k < kHostStreams && ok; ++k)
     ok = cudaStreamWaitEvent(hs[k], ev_start, 0) == cudaSuccess;
+  if (by_time && ok) {
+    // Slice k holds steps [t0, t0 + Lk) of every batch row, staged densely as (batch, Lk, dim);
+    // its scan waits for slice k - 1's (sscan_fwd_ex from its end state, in place in dh), while
+    // the copies of neighbouring slices run on the other streams in both directions.
+    const int64_t n_t = std::min<int64_t>(kHostTimeSlices, L / kHostMinSliceSteps);
+    const int64_t Ls = (L + n_t - 1) / n_t;
+    cudaEvent_t ev_scan[kHostTimeSlices] = {};
+    for (int64_t k = 0; k < n_t && ok; ++k)
+      ok = cudaEventCreateWithFlags(&ev_scan[k], cudaEventDisableTiming) == cudaSuccess;
+    const unsigned char* hu = static_cast<const unsigned char*>(u);
+    const unsigned char* hdl = static_cast<const unsigned char*>(delta);
+    const unsigned char* hz = static_cast<const unsigned char*>(z);
+    const unsigned char* hB = static_cast<const unsigned char*>(B);
+    const unsigned char* hC = static_cast<const unsigned char*>(C);
+    unsigned char* hy = static_cast<unsigned char*>(y);
+    const size_t row_d = size_t(L * dim) * es, row_n = size_t(L * N) * es;  // host row pitches
+    auto copy2 = [&](void* dst, size_t dp, const void* src, size_t sp, size_t w,
+                     cudaMemcpyKind kind, cudaStream_t s) {
+      return cudaMemcpy2DAsync(dst, dp, src, sp, w, size_t(batch), kind, s) == cudaSuccess;
+    };
+    for (int64_t k = 0, t0 = 0; k < n_t && t0 < L && ok; ++k, t0 += Ls) {
+      const int64_t Lk = std::min(Ls, L - t0);
+      cudaStream_t s = hs[k % kHostStreams];
+      const size_t od = size_t(batch * t0 * dim) * es, on = size_t(batch * t0 * N) * es;
+      const size_t wd = size_t(Lk * dim) * es, wn = size_t(Lk * N) * es;  // one row's slice
+      const size_t hd = size_t(t0 * dim) * es, hn = size_t(t0 * N) * es;  // its host offset
+      ok = copy2(du + od, wd, hu + hd, row_d, wd, H2D, s) &&
+           copy2(ddl + od, wd, hdl + hd, row_d, wd, H2D, s) &&
+           (!z || copy2(dz + od, wd, hz + hd, row_d, wd, H2D, s)) &&
+           copy2(dB + on, wn, hB + hn, row_n, wn, H2D, s) &&
+           copy2(dC + on, wn, hC + hn, row_n, wn, H2D, s);
+      if (ok && k > 0) ok = cudaStreamWaitEvent(s, ev_scan[k - 1], 0) == cudaSuccess;
+      if (ok) {
+        st = sscan_fwd_ex(du + od, ddl + od, dA, dB + on, dC + on, dD, z ? dz + od : nullptr,
+                          dbias, softplus_flag, k > 0 ? dh : nullptr, SSCAN_DISC_ZOH, dy + od,
+                          dh, batch, Lk, dim, N, dtype, s);
+        ok = st == SSCAN_OK;
+      }
+      ok = ok && cudaEventRecord(ev_scan[k], s) == cudaSuccess &&
+           copy2(hy + hd, row_d, dy + od, wd, wd, D2H, s);
+      if (ok && h_last && t0 + Lk == L)
+        ok = copy(h_last, dh, size_t(batch * dim * N) * 4, D2H, s);
+    }
+    for (int k = 0; k < kHostStreams; ++k) {  // every stream done before the events go
+      if (ok) ok = cudaEventRecord(ev_done[k], hs[k]) == cudaSuccess &&
+                   cudaStreamWaitEvent(stream, ev_done[k], 0) == cudaSuccess;
+    }
+    if (ok) ok = cudaStreamSynchronize(stream) == cudaSuccess;
+    if (!ok)
+      for (int k = 0; k < kHostStreams; ++k) cudaStreamSynchronize(hs[k]);
+    for (int64_t k = 0; k < n_t; ++k)
+      if (ev_scan[k]) cudaEventDestroy(ev_scan[k]);
+    if (ev_start) cudaEventDestroy(ev_start);
+    for (int k = 0; k < kHostStreams; ++k)
+      if (ev_done[k]) cudaEventDestroy(ev_done[k]);
+    if (!ok) return st != SSCAN_OK ? st : SSCAN_ERR_CUDA;
+    return SSCAN_OK;
+  }
   const int64_t n_slices = batch < kHostSlices ? batch : kHostSlices;
   const int64_t rows = (batch + n_slices - 1) / n_slices;
   const unsigned char* hu = static_cast<const unsigned char*>(u);

@@ -198,6 +198,21 @@ def test_host_entry_many_slices(io):
     assert_within(compare(yh, hh, yr, hr, w.io, y_mag=ym), w.io, f"host entry, 19 rows, {io}")
 
 
+@pytest.mark.parametrize("io,batch", [("f32", 1), ("bf16", 3)])
+def test_host_entry_time_slices(io, batch):
+    """Few batch rows and a long sequence: the host entry cuts the sequence into time slices
+    (each continuing from the previous one's end state, staged as dense (batch, slice, dim)
+    blocks by strided copies), against the oracle over the whole sequence."""
+    base = WORKLOADS["fp32"] if io == "f32" else WORKLOADS["bf16"]
+    w = base.replace(batch=batch, L=50001, dim=24)
+    x = make_inputs(w, device=DEV)
+    xc = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+    yh, hh = binding.fwd_host(xc["u"], xc["delta"], xc["A"], xc["B"], xc["C"], xc["D"], xc["z"],
+                              xc["delta_bias"])
+    yr, hr, ym = oracle_full(x)
+    assert_within(compare(yh, hh, yr, hr, w.io, y_mag=ym), w.io, f"host entry, time slices, {io}")
+
+
 def test_invalid_arguments_rejected_synchronously():
     w = WORKLOADS["fp32"].replace(batch=1, L=8, dim=64)
     x = make_inputs(w, device=DEV)
