@@ -72,6 +72,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["lib", "reference"], default="lib")
     ap.add_argument("--workload", default="long")
     ap.add_argument("--L", type=int, default=0, help="override the workload's L (profiling)")
+    ap.add_argument("--dim", type=int, default=0,
+                    help="override the workload's channel count D (profiling)")
     ap.add_argument("--no-configs", action="store_true",
                     help="time only the headline workload")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -700,6 +702,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.L:
         w = w.replace(L=args.L)
+    if args.dim:
+        w = w.replace(dim=args.dim)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -791,7 +795,8 @@ def main():
     sec_per_step = ms_max / 1e3 / args.steps
     value = whole_job_rate(w.elems, world, sec_per_step)
     roof = scan_roofline(w, sec_per_step, upeak, hbm_gbs, peak_src,
-                         recorded_traffic(args.workload), clocks)
+                         recorded_traffic(args.workload) if not (args.L or args.dim) else None,
+                         clocks)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
