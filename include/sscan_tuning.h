@@ -36,7 +36,7 @@ typedef struct {
                             out and report SSCAN_ERR_CARRY_TIMEOUT (-1: off) */
   int time_scan;         /* forward: 1 = the time-lane kernel (a warp scans one channel over
                             time, the lanes' aggregates composed in order), 2 = never, 0 = auto
-                            (at most 32 channels, or at most 128 channels and 2^24 channel-steps,
+                            (at most 64 channels, or at most 256 channels and 2^23 channel-steps,
                             unless states_per_lane, threads or chunk is set); calls that write
                             backward checkpoints never use it */
 } sscan_tuning_t;

@@ -771,6 +771,7 @@ constexpr int kTsT = 8;               // steps per lane and chunk
 constexpr int kTsChunk = 32 * kTsT;   // steps per chunk
 constexpr int kTsW = 8;               // warps (channels) per CTA
 constexpr int kTsPad = kTsT + 1;      // float4 slots per lane and quad of states (one pad)
+constexpr int kTsScan = kNP + 4;      // floats per lane of the aggregate rows (16 + pad)
 
 struct TsSmem {
   size_t tile_io, bc, stage, off_t, t_io, off_bt, bt, off_scan, scan_warp, off_y, y_tile, off_bar,
@@ -784,10 +785,10 @@ struct TsSmem {
     off_bt = off_t + 3 * t_io;                              // B, C as [4][32][kTsPad] float4
     bt = align128(size_t(4) * 32 * kTsPad * 4 * sizeof(float));
     off_scan = off_bt + 2 * bt;
-    scan_warp = align128(2 * 32 * kNP * sizeof(float));  // P, H [32][16]
-    off_y = off_scan + size_t(kTsW) * scan_warp;         // two y tiles [kTsChunk][kTsW]
+    scan_warp = align128(2 * 32 * kTsScan * sizeof(float));  // P, H [32][kTsScan]
+    off_y = off_scan + size_t(kTsW) * scan_warp;             // the y tile [kTsChunk][kTsW]
     y_tile = align128(size_t(kTsChunk) * kTsW * es);
-    off_bar = off_y + 2 * y_tile;
+    off_bar = off_y + y_tile;
     total = off_bar + 8 * 8;  // full[8]
   }
 };
@@ -932,8 +933,8 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
   const float hz = (p.h0 && live && lane < N) ? p.h0[(size_t(b) * p.dim + cg) * N + lane] : 0.f;
   float carry = seg == 0 ? hz : 0.f;
   float* scanP = reinterpret_cast<float*>(smem + lay.off_scan + size_t(warp) * lay.scan_warp);
-  float* scanH = scanP + 32 * kNP;
-  IO* ytile0 = reinterpret_cast<IO*>(smem + lay.off_y);
+  float* scanH = scanP + 32 * kTsScan;
+  IO* ytile = reinterpret_cast<IO*>(smem + lay.off_y);
   const float4* bq_l = tB + lane * kTsPad;  // this lane's B, C slots: quad qd at + qd 32 kTsPad
   const float4* cq_l = tC + lane * kTsPad;
 
@@ -1071,8 +1072,9 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
           P0 = f2(ex2(A2[r].x * ssum), ex2(A2[r].y * ssum));
           P1 = f2(ex2(A2[r + 1].x * ssum), ex2(A2[r + 1].y * ssum));
         }
-        *reinterpret_cast<float4*>(scanP + lane * kNP + 2 * r) = make_float4(P0.x, P0.y, P1.x, P1.y);
-        *reinterpret_cast<float4*>(scanH + lane * kNP + 2 * r) =
+        *reinterpret_cast<float4*>(scanP + lane * kTsScan + 2 * r) =
+            make_float4(P0.x, P0.y, P1.x, P1.y);
+        *reinterpret_cast<float4*>(scanH + lane * kTsScan + 2 * r) =
             make_float4(h[r].x, h[r].y, h[r + 1].x, h[r + 1].y);
       }
       if (!readout) {  // the chunk's summed step (a fixed tree), into the segment's Kahan sum
@@ -1086,13 +1088,14 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
       }
       __syncwarp();
       // 2. Compose the 32 aggregates of state n in order (lane n < 16), from the carry; every
-      //    lane's start state replaces its P.
+      //    lane's start state replaces its P. (Splitting the walk into two halves of 16, the
+      //    second fixed up with the first's end state, measured slower.)
       if (scanner) {
         float x = carry;
 #pragma unroll 8
         for (int j = 0; j < 32; ++j) {
-          const float pj = scanP[j * kNP + lane], hj = scanH[j * kNP + lane];
-          scanP[j * kNP + lane] = x;
+          const float pj = scanP[j * kTsScan + lane], hj = scanH[j * kTsScan + lane];
+          scanP[j * kTsScan + lane] = x;
           x = fmaf(pj, x, hj);
           if constexpr (EULER) {
             if (!readout) pprod *= pj;
@@ -1106,7 +1109,7 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
         //    slots of the regrouped u (read above), then regrouped into the TMA tile.
 #pragma unroll
         for (int r = 0; r < KP; r += 2) {
-          const float4 hv = *reinterpret_cast<const float4*>(scanP + lane * kNP + 2 * r);
+          const float4 hv = *reinterpret_cast<const float4*>(scanP + lane * kTsScan + 2 * r);
           h[r] = f2(hv.x, hv.y);
           h[r + 1] = f2(hv.z, hv.w);
         }
@@ -1130,20 +1133,19 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
           yv[k] = fmaf(D_c, uo[k], acc.x + acc.y) * sil[k];
         }
         store8(tU + warp * kTsChunk + row0, yv);
-        __syncthreads();  // every warp's y is in tU
-        IO* yt = ytile0 + size_t(ystores & 1) * (lay.y_tile / sizeof(IO));
+        if (tid == 0 && ystores > 0) tma_store_wait_read<0>();  // the last tile has been read
+        __syncthreads();  // every warp's y is in tU, and the y tile is free
         {
           float v[8];
 #pragma unroll
           for (int w = 0; w < kTsW; ++w) v[w] = to_f32(tU[w * kTsChunk + tid]);
-          store8(yt + tid * kTsW, v);
+          store8(ytile + tid * kTsW, v);
         }
         fence_smem_to_async();  // this thread's y row before the tile's TMA store
         __syncthreads();
         if (tid == 0) {
-          tma_store_3d(&tm_y, yt, ch0, t0, b);
+          tma_store_3d(&tm_y, ytile, ch0, t0, b);
           tma_store_commit();
-          tma_store_wait_read<1>();  // the other tile, written next, has been read
         }
         ++ystores;
       }
@@ -1527,17 +1529,17 @@ static cudaError_t launch_tscan(const FwdArgs& a, const Tuning& tune) {
 
 // The time-lane kernel: when asked for, or automatically for few channels, where the lane
 // kernel's many short time segments are bound by the chain of segment prefixes. Measured on
-// B300 (bf16, batch 1; lane kernel -> time lanes): D 8, L 2^20 1.42 -> 0.72 ms; D 32, L 2^20
-// 1.44 -> 0.89 ms; D 64, L 2^18 0.57 -> 0.44 ms; D 64, L 2^20 1.46 -> 1.59 ms; D 128, L 2^16
-// 0.29 -> 0.22 ms; D 128, L 2^18 0.74 -> 0.97 ms: time lanes for at most 32 channels, or at
-// most 128 channels and 2^24 channel-steps. It writes no backward checkpoints, and an explicit
+// B300 (bf16, batch 1; lane kernel -> time lanes): D 32, L 2^20 1.45 -> 0.80 ms; D 64, L 2^20
+// 1.45 -> 1.40 ms; D 128, L 2^16 0.29 -> 0.22 ms; D 128, L 2^18 0.75 -> 0.85 ms; D 256, L 2^14
+// 0.152 -> 0.107 ms; D 256, L 2^16 0.35 -> 0.41 ms: time lanes for at most 64 channels, or at
+// most 256 channels and 2^23 channel-steps. It writes no backward checkpoints, and an explicit
 // lane layout (states per lane, threads, chunk) keeps the lane kernel.
 static bool use_tscan(const FwdArgs& a, const Tuning& tune) {
   if (a.h_ckpt || tune.time_scan == 2) return false;
   if (tune.time_scan == 1) return true;
   if (tune.states_per_lane || tune.threads || tune.chunk) return false;
   const int64_t chans = a.batch * a.dim;
-  return chans <= 128 && (chans <= 32 || chans * a.L <= (int64_t(1) << 24));
+  return chans <= 64 || (chans <= 256 && chans * a.L <= (int64_t(1) << 23));
 }
 
 cudaError_t launch_tma(const FwdArgs& a, const Tuning& tune) {
