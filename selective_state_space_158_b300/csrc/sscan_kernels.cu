@@ -1498,7 +1498,29 @@ cudaError_t launch_lane(const FwdArgs& a, const Tuning& tune) {
     G = chans >= 24576 ? 1 : (chans >= 16384 ? 2 : 4);
     if (chans * 4 / 32 < kSplitBelowWarps) G = 2;
   }
-  const int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
+  int threads = tune.threads ? tune.threads : (G == 1 ? 256 : (G == 2 ? 128 : 64));
+  if (!tune.threads && G >= 2 && tune.segments <= 1) {
+    // Two or four lanes per channel in one wave (no time split): the CTA size that puts the
+    // fewest warps on the busiest SM when the CTAs spread evenly over the 148 SMs, the larger
+    // CTA on a tie. Measured on B300: wide bf16 b4 L8192 D5120 1.127 ms with 4 warps per CTA
+    // (12 on the busiest SM), 1.094 ms with 3 (9); fp32 b8 L2048 D1536 0.202 ms with 2 warps
+    // (12), 0.196 ms with 1 (11).
+    const int CPWl = 32 / G;
+    const int64_t warps = a.batch * ((a.dim + CPWl - 1) / CPWl);
+    if (warps >= kSplitBelowWarps) {
+      int best_w = threads / 32;
+      int64_t best = INT64_MAX;
+      for (int w = threads / 32; w >= 1; --w) {
+        const int64_t ctas = a.batch * ((a.dim + int64_t(w) * CPWl - 1) / (int64_t(w) * CPWl));
+        const int64_t busiest = (ctas + 147) / 148 * w;
+        if (busiest < best) {
+          best = busiest;
+          best_w = w;
+        }
+      }
+      threads = 32 * best_w;
+    }
+  }
   if (threads % 32 || threads < 32 || threads > 256) return cudaErrorInvalidValue;
   const int es = a.io == Io::F32 ? 4 : 2;
   if (G != 1 && G != 2 && G != 4) return cudaErrorInvalidValue;
