@@ -1434,9 +1434,13 @@ cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, const Tuning& tu
                      : launch_lane_typed<IO, 4, 16, EULER>(a, threads, tune);
 }
 
-// The time-lane kernel: CTAs of kTsW channels; for few channels the sequence is split into
-// about two CTAs per SM in total, capped by the chain of segment prefixes (sqrt(L / 10), as for
-// the lane kernel).
+// The time-lane kernel: CTAs of kTsW channels (one resident per SM); for few channels the
+// sequence is split into time segments: one wave of CTAs when a segment has at most 4 CTAs, two
+// waves otherwise, and at most sqrt(L / 80) segments, where the chain of segment prefixes
+// (about 2.4 us a segment) overtakes a segment's own work. Measured on B300 (bf16, batch 1):
+// D 8, L 2^20: 296 segments (two waves) 0.72 ms, 148 0.52 ms, 74 0.54 ms; D 16, L 2^18: 148
+// segments 0.35 ms, 74 0.25 ms; D 8, L 2^16: 64 segments 0.157 ms, 37 0.124 ms; D 64, L 2^20:
+// 37 segments (two waves) 1.40 ms, 18 (one) 1.43 ms.
 template <typename IO, bool EULER>
 cudaError_t launch_tscan_typed(const FwdArgs& a, const Tuning& tune) {
   const int es = int(sizeof(IO));
@@ -1451,8 +1455,9 @@ cudaError_t launch_tscan_typed(const FwdArgs& a, const Tuning& tune) {
   if (segments <= 0) {
     segments = 1;
     if (ctas_per_seg < 148) {
-      const double fill = std::ceil(2.0 * 148.0 / double(ctas_per_seg));
-      segments = int(std::max(1.0, std::min(fill, std::ceil(std::sqrt(double(a.L) / 10.0)))));
+      const double fill = ctas_per_seg <= 4 ? std::floor(148.0 / double(ctas_per_seg))
+                                            : std::ceil(296.0 / double(ctas_per_seg));
+      segments = int(std::max(1.0, std::min(fill, std::ceil(std::sqrt(double(a.L) / 80.0)))));
     }
   }
   LaneParams p = base_params(a, kTsW, stages, segments, 0, tune.skip_publish, kTsChunk);
