@@ -166,6 +166,15 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+constexpr uint32_t kTsLookbackTries = 1u << 26;  // a cap beside the one-second time bound
 __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -949,25 +958,33 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
   for (int pass = agg_pass ? 0 : 1; pass < 2 && !timed_out; ++pass) {
     const bool readout = pass == 1;
     if (readout && p.n_seg > 1) {
-      // Chunk carry between segments, as in the lane kernel: segment s > 0 waits for segment
-      // s - 1's inclusive prefix and, with a successor, publishes its own,
-      // 2^(A log2e SD_s) h_in + H_s (the product of its factors for the first order).
+      // Chunk carry between segments: segment s > 0 waits for segment s - 1's inclusive prefix
+      // and, with a successor, publishes its own, 2^(A log2e SD_s) h_in + H_s (the product of
+      // its factors for the first order). Each state's prefix is one 64-bit word, its value
+      // and a valid bit, stored and read whole (zeroed before the launch), so a lane polls its
+      // own word and no fence or separate flag sits on the chain from segment to segment.
+      unsigned long long* words = reinterpret_cast<unsigned long long*>(p.agg);
       float start = hz;
       if (seg > 0) {
         const size_t up = unit - units_per_seg;
-        unsigned f = 0;
-        if (lane == 0) {
-          for (uint32_t it = 0; it < kLookbackTries; ++it) {
-            f = ld_acquire(p.flags + up);
-            if (f != 0) break;
-            __nanosleep(512);
+        bool got = !scanner;
+        if (scanner) {  // bounded: about a second of polling
+          const uint64_t t_begin = globaltimer_ns();
+          for (uint32_t it = 0; it < kTsLookbackTries; ++it) {
+            const unsigned long long v = ld_relaxed_u64(words + up * kNP + lane);
+            if (v >> 32) {
+              start = __uint_as_float(unsigned(v));
+              got = true;
+              break;
+            }
+            if (globaltimer_ns() - t_begin > kWaitNs) break;
+            __nanosleep(64);
           }
-          if (f == 0) atomicOr(p.status, kErrCarry);
+          if (!got) start = 0.f;  // timed out: the status word says the result is wrong
         }
-        f = __shfl_sync(0xffffffffu, f, 0);
-        start = (f != 0 && scanner) ? __ldcg(p.agg + up * kNP + lane) : 0.f;
+        if (__any_sync(0xffffffffu, !got) && lane == 0) atomicOr(p.status, kErrCarry);
       }
-      if (agg_pass && seg != p.skip_publish) {
+      if (agg_pass && seg != p.skip_publish && scanner) {
         float incl = carry;  // segment 0: the end state from h0 already
         if (seg > 0) {
           float P;
@@ -979,10 +996,8 @@ __global__ void __launch_bounds__(kTsW * 32, 1)
             P = ex2(a_n * sd);
           incl = fmaf(P, start, carry);
         }
-        if (scanner) p.agg[unit * kNP + lane] = incl;
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release(p.flags + unit, kFlagAgg);
+        st_relaxed_u64(words + unit * kNP + lane,
+                       (1ull << 32) | (unsigned long long)__float_as_uint(incl));
       }
       carry = start;
     }
@@ -1259,7 +1274,8 @@ struct Workspace {
   }
 };
 
-cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Workspace* w) {
+cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Workspace* w,
+                              bool zero_carry = false) {
   w->stream = a.stream;
   const bool widen = a.io != Io::F32 || a.N != kNP;
   const size_t rows = size_t(a.batch) * size_t(a.L);
@@ -1306,7 +1322,7 @@ cudaError_t prepare_workspace(const FwdArgs& a, size_t carry_units, int K, Works
   }
   if (carry_units) {
     char* carry = wsb + 2 * bc_bytes;
-    e = cudaMemsetAsync(carry, 0, flag_bytes, a.stream);
+    e = cudaMemsetAsync(carry, 0, zero_carry ? carry_bytes : flag_bytes, a.stream);
     if (e != cudaSuccess) return w->release(e);
     w->ticket = reinterpret_cast<unsigned*>(carry);
     w->flags = w->ticket + 1;
@@ -1436,11 +1452,10 @@ cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, const Tuning& tu
 
 // The time-lane kernel: CTAs of kTsW channels (one resident per SM); for few channels the
 // sequence is split into time segments: one wave of CTAs when a segment has at most 4 CTAs, two
-// waves otherwise, and at most sqrt(L / 80) segments, where the chain of segment prefixes
-// (about 2.4 us a segment) overtakes a segment's own work. Measured on B300 (bf16, batch 1):
-// D 8, L 2^20: 296 segments (two waves) 0.72 ms, 148 0.52 ms, 74 0.54 ms; D 16, L 2^18: 148
-// segments 0.35 ms, 74 0.25 ms; D 8, L 2^16: 64 segments 0.157 ms, 37 0.124 ms; D 64, L 2^20:
-// 37 segments (two waves) 1.40 ms, 18 (one) 1.43 ms.
+// waves otherwise, and at most sqrt(L / 32) segments, where the chain of segment prefixes
+// (about 1 us a segment) overtakes a segment's own work. Measured on B300 (bf16, batch 1):
+// D 8, L 2^20: 148 segments (one wave) 0.31 ms, 296 (two) 0.31 ms, 222 0.33 ms; D 8, L 2^16:
+// 46 segments 0.068 ms; D 64, L 2^20: 37 segments 1.37 ms.
 template <typename IO, bool EULER>
 cudaError_t launch_tscan_typed(const FwdArgs& a, const Tuning& tune) {
   const int es = int(sizeof(IO));
@@ -1457,13 +1472,13 @@ cudaError_t launch_tscan_typed(const FwdArgs& a, const Tuning& tune) {
     if (ctas_per_seg < 148) {
       const double fill = ctas_per_seg <= 4 ? std::floor(148.0 / double(ctas_per_seg))
                                             : std::ceil(296.0 / double(ctas_per_seg));
-      segments = int(std::max(1.0, std::min(fill, std::ceil(std::sqrt(double(a.L) / 80.0)))));
+      segments = int(std::max(1.0, std::min(fill, std::ceil(std::sqrt(double(a.L) / 32.0)))));
     }
   }
   LaneParams p = base_params(a, kTsW, stages, segments, 0, tune.skip_publish, kTsChunk);
   Workspace w;
   cudaError_t e = prepare_workspace(
-      a, p.n_seg > 1 ? size_t(p.n_seg) * size_t(ctas_per_seg) * kTsW : 0, 1, &w);
+      a, p.n_seg > 1 ? size_t(p.n_seg) * size_t(ctas_per_seg) * kTsW : 0, 1, &w, true);
   if (e != cudaSuccess) return e;
   p.ticket = w.ticket;
   p.flags = w.flags;
