@@ -256,7 +256,7 @@ __host__ __device__ constexpr int lane_min_blocks() {
   return G == 4 ? (TC == 32 ? 3 : 2) : (G == 2 ? (std::is_same<IO, float>::value ? 3 : 4) : 1);
 }
 
-template <typename IO, int G, int TC, bool EULER>
+template <typename IO, int G, int TC, bool EULER, bool CKPT>
 __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO, G, TC>())
     sscan_lane_kernel(
     const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dl,
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(lane_max_threads<G, TC>(), lane_min_blocks<IO,
         break;
       }
 
-      if (readout && p.h_ckpt && live) {  // the state before this chunk (backward pass)
+      if (CKPT && readout && live) {  // the state before this chunk (backward pass)
         float* dst = p.h_ckpt + ((size_t(c) * p.batch + b) * p.dim + cg) * N;
         if (KP % 2 == 0 && (N & 3) == 0) {  // 16-byte stores: n0 and N are multiples of 4
 #pragma unroll
@@ -1381,7 +1381,7 @@ LaneParams base_params(const FwdArgs& a, int CH, int stages, int segments, int64
   return p;
 }
 
-template <typename IO, int G, int TC, bool EULER>
+template <typename IO, int G, int TC, bool EULER, bool CKPT>
 cudaError_t launch_lane_typed(const FwdArgs& a, int threads, const Tuning& tune) {
   threads = std::min(threads, lane_max_threads<G, TC>());  // the kernel's launch bound
   int stages = tune.stages;
@@ -1426,7 +1426,7 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, const Tuning& tune)
             make_map(&mC, w.C16, Io::F32, kNP, L, bt, kNP, TC) &&
             make_map(&my, a.y, a.io, dim, L, bt, CPW, TC);
   if (!ok) return w.release(cudaErrorInvalidValue);
-  auto kern = sscan_lane_kernel<IO, G, TC, EULER>;
+  auto kern = sscan_lane_kernel<IO, G, TC, EULER, CKPT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return w.release(e);
   if (p.n_seg > 1) {
@@ -1443,11 +1443,19 @@ cudaError_t launch_lane_typed(const FwdArgs& a, int threads, const Tuning& tune)
 // few state updates per step), else 16; always 16 when the backward pass wants checkpoints.
 template <typename IO, bool EULER>
 cudaError_t launch_lane_g(const FwdArgs& a, int G, int threads, const Tuning& tune) {
-  if (G == 1) return launch_lane_typed<IO, 1, 16, EULER>(a, threads, tune);
-  if (G == 2) return launch_lane_typed<IO, 2, 16, EULER>(a, threads, tune);
+  // Backward checkpoints get their own instantiations (the store code left out of the others
+  // measured 0.3-1.6% faster on the forward workloads).
+  const bool ck = a.h_ckpt != nullptr;
+  if (G == 1)
+    return ck ? launch_lane_typed<IO, 1, 16, EULER, true>(a, threads, tune)
+              : launch_lane_typed<IO, 1, 16, EULER, false>(a, threads, tune);
+  if (G == 2)
+    return ck ? launch_lane_typed<IO, 2, 16, EULER, true>(a, threads, tune)
+              : launch_lane_typed<IO, 2, 16, EULER, false>(a, threads, tune);
   const bool long_chunks = !a.h_ckpt && tune.chunk != 16 && threads <= 128;
-  return long_chunks ? launch_lane_typed<IO, 4, 32, EULER>(a, threads, tune)
-                     : launch_lane_typed<IO, 4, 16, EULER>(a, threads, tune);
+  if (long_chunks) return launch_lane_typed<IO, 4, 32, EULER, false>(a, threads, tune);
+  return ck ? launch_lane_typed<IO, 4, 16, EULER, true>(a, threads, tune)
+            : launch_lane_typed<IO, 4, 16, EULER, false>(a, threads, tune);
 }
 
 // The time-lane kernel: CTAs of kTsW channels (one resident per SM); for few channels the
