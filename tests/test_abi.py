@@ -78,3 +78,28 @@ def test_argument_errors_are_synchronous_without_a_device(lib):
         args = list(ok_cv)
         args[idx] = val
         assert lib.sscan_conv1d_silu(*args) == 1, (idx, val)
+
+
+def test_tuning_ranges_are_checked_without_a_device(lib):
+    """sscan_set_tuning refuses out-of-range fields and leaves the setting unchanged; the
+    setting round-trips through sscan_get_tuning; NULL restores every automatic choice."""
+    T = binding.Tuning
+    bad = [dict(states_per_lane=3), dict(threads=48), dict(threads=288), dict(stages=1),
+           dict(stages=9), dict(chunk=8), dict(ctas_per_sm=33), dict(test_skip_publish=-2),
+           dict(time_scan=3), dict(time_scan=-1), dict(segments=-1)]
+    for fields in bad:
+        t = T(test_skip_publish=-1)
+        for k, v in fields.items():
+            setattr(t, k, v)
+        assert lib.sscan_set_tuning(ctypes.byref(t)) == 1, fields
+    good = T(states_per_lane=8, segments=3, threads=96, stages=4, chunk=16, ctas_per_sm=2,
+             test_skip_publish=-1, time_scan=2)
+    assert lib.sscan_set_tuning(ctypes.byref(good)) == 0
+    back = T()
+    assert lib.sscan_get_tuning(ctypes.byref(back)) == 0
+    for name, _ in T._fields_:
+        assert getattr(back, name) == getattr(good, name), name
+    assert lib.sscan_set_tuning(None) == 0
+    assert lib.sscan_get_tuning(ctypes.byref(back)) == 0
+    assert (back.states_per_lane, back.segments, back.time_scan, back.test_skip_publish) == \
+        (0, 0, 0, -1)
